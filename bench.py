@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of the BitNet b1.58 BitLinear forward on B300.
+
+Headline workload: decode through the BitLinear projections of a 2B-class
+BitNet b1.58 (hidden 2560, FFN 6912; QKV 2560->3840, O 2560->2560, gate+up
+2560->2x6912, down 6912->2560) at M = 1 and M = 8 tokens, over 30 layers of
+distinct weights (520 MB of packed weights per pass, more than 4x the 126 MB
+L2, so no pass is served from L2).  One step = for M in (1, 8): for each layer
+and projection: RMSNorm + int8 quantization of the input, then the ternary
+contraction with fused dequantization (bitlinear_quant_act + bitlinear_forward).
+Weights are packed once before timing (offline step).
+
+Metric: packed-weight GB/s (packed bytes streamed per step / step time).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun); value is
+the aggregate over ranks and the step time the max over ranks.  The reference
+arm times the CPU oracle (the plain single-threaded C definition) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BitLinear decode packed-weight GB/s vs HBM peak; M=2048 prefill int8 TOPS"
+WORKLOAD = "decode_2b"
+LAYERS = 30
+RMS_EPS = 1e-5
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6400.0, 1800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons while the timed region runs: NVML
+    (pynvml) polled every ~2 ms when importable, else `nvidia-smi -lms 50`."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks",
+               0x100: "display_clock", 0x10: "sync_boost"}
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples, self.reasons, self.names, self.mode = [], 0, set(), None
+        self.max_mhz = None
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM))
+            self.mode = "nvml"
+        except Exception:
+            self.mode = "smi"
+
+    def _sample(self):
+        nv = self.nv
+        self.samples.append(float(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)))
+        self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.mode == "nvml":
+            self._sample()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        else:
+            import subprocess
+            import tempfile
+            self._f = tempfile.TemporaryFile(mode="w+")
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+            try:
+                self._p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                            "-i", str(self.index), "-lms", "50"], stdout=self._f,
+                                           stderr=subprocess.DEVNULL)
+                time.sleep(0.3)
+            except Exception:
+                self._p = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.mode == "nvml":
+            self._stop.set()
+            self._t.join()
+            self._sample()
+        elif self._p is not None:
+            time.sleep(0.1)
+            self._p.terminate()
+            self._p.wait()
+            self._f.seek(0)
+            labels = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in self._f.read().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for lab, v in zip(labels, f[2:6]):
+                    if v.lower() == "active":
+                        self.names.add(lab)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": self.mode}
+        names = set(self.names) | {n for b, n in self.REASONS.items() if self.reasons & b}
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(names), "samples": len(self.samples), "source": self.mode}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+
+_ORACLE_SAMPLE = None
+
+
+def _oracle_inputs():
+    """Layer 0 of the decode workload, ternarized by the oracle (offline step, not timed)."""
+    global _ORACLE_SAMPLE
+    if _ORACLE_SAMPLE is None:
+        import oracle
+        from bitlinear_rmsnorm_token_int8_b300 import synth
+        wl = synth.WORKLOADS[WORKLOAD]
+        mats = []
+        for pi, p in enumerate(wl.projections):
+            W = synth.latent_weights(p.N, p.K, synth.weight_seed(wl.seed, 0, pi)).numpy()
+            _, gamma, wq = oracle.pack_weights(W)
+            mats.append((p, gamma, wq))
+        xs = {}
+        for M in wl.tokens:
+            for K in sorted({p.K for p in wl.projections}):
+                xs[(M, K)] = (synth.bf16_bits(synth.activations(M, K, synth.act_seed(wl.seed, M, K), outliers=False)),
+                              synth.bf16_bits(synth.rms_gains(K, synth.gain_seed(wl.seed, 0, K))))
+        _ORACLE_SAMPLE = (wl, mats, xs)
+    return _ORACLE_SAMPLE
+
+
+def oracle_sample(seconds: float = 12.0):
+    """Times the CPU oracle as it stands (act-quant + add/skip/subtract contraction +
+    dequant) on layer 0 of the decode workload at M = 1 and M = 8, whole passes
+    repeated until ~`seconds` have passed.  Returns (packed-weight GB/s, seconds, passes)."""
+    import oracle
+    wl, mats, xs = _oracle_inputs()
+    done_bytes, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        for M in wl.tokens:
+            for p, gamma, wq in mats:
+                xb, gb = xs[(M, p.K)]
+                xq, sig = oracle.act_quant(xb, gb, RMS_EPS)
+                acc = oracle.ternary_matmul(xq, wq)
+                oracle.dequant(acc, sig, np.full(p.N, float(gamma)))
+                done_bytes += p.N * p.K // 4
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return done_bytes / el / 1e9, el, reps
+
+
+def reference_arm(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    _oracle_inputs()
+    per_step = min(args.ref_seconds, 150.0 / max(args.steps, 1))   # whole arm within a few minutes
+    t0 = time.perf_counter()
+    gbs_list = []
+    for _ in range(args.steps):
+        gbs, _, _ = oracle_sample(per_step)
+        gbs_list.append(gbs)
+    el = time.perf_counter() - t0
+    value = float(statistics.mean(gbs_list))
+    sample = (f"layer 0 of {LAYERS} (QKV, O, gate+up, down) at M=1 and M=8 per step, "
+              f"~{per_step:.1f} s per step, single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "layers_sampled": 1, "tokens": [1, 8]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def traffic_record(kernel_src: str):
+    """ncu DRAM bytes per launch recorded for the current source of the kernel, or None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    r = rec.get(WORKLOAD)
+    if not r or r.get("source_sha") != sha:
+        return None
+    return float(r["dram_bytes_per_launch"])
+
+
+def our_arm(args):
+    import torch
+    import bitlinear_rmsnorm_token_int8_b300 as bl
+    from bitlinear_rmsnorm_token_int8_b300 import synth
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    bl.lib()
+    wl = synth.WORKLOADS[WORKLOAD]
+    layers = args.layers
+
+    # ---- weights (offline step, not timed)
+    weights = []
+    for layer in range(layers):
+        row = []
+        for pi, p in enumerate(wl.projections):
+            W = synth.latent_weights_device(p.N, p.K, synth.weight_seed(wl.seed, layer, pi) + 7919 * rank, dev)
+            packed, w_scale, _ = bl.bitlinear_pack_weights(W)
+            del W
+            row.append((p, packed, w_scale))
+        weights.append(row)
+    torch.cuda.synchronize()
+    assert bl.bitlinear_get_device_error() == 0
+
+    # ---- activations and buffers
+    Ks = sorted({p.K for p in wl.projections})
+    xs, gains, xq, sc, ys = {}, {}, {}, {}, {}
+    for K in Ks:
+        gains[K] = synth.rms_gains(K, synth.gain_seed(wl.seed, 0, K)).to(dev)
+    for M in wl.tokens:
+        for K in Ks:
+            xs[(M, K)] = synth.activations(M, K, synth.act_seed(wl.seed, M, K), outliers=False).to(dev)
+            xq[(M, K)] = torch.empty((M, K), dtype=torch.int8, device=dev)
+            sc[(M, K)] = torch.empty(M + 4, dtype=torch.float32, device=dev)[:M]
+        for p in wl.projections:
+            ys[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+    fwd_ws = {}
+    for M in wl.tokens:
+        for p in wl.projections:
+            need = bl.bitlinear_forward_workspace_bytes(M, p.N, p.K)
+            fwd_ws[(M, p.N, p.K)] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+
+    packed_bytes_step = sum(p.N * p.K // 4 for _ in wl.tokens for row in weights for (p, _, _) in row)
+    alg_bytes_fwd = []     # algorithmic bytes of each forward launch, in launch order
+    for M in wl.tokens:
+        for row in weights:
+            for (p, _, _) in row:
+                alg_bytes_fwd.append(p.N * p.K // 4 + M * p.K + 4 * M + 4 * p.N + 2 * M * p.N)
+
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        i = 0
+        for M in wl.tokens:
+            for row in weights:
+                for (p, packed, w_scale) in row:
+                    bl.bitlinear_quant_act(xs[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)], act_scale=sc[(M, p.K)])
+                    if ev is not None:
+                        ev[i][0].record(stream)
+                    bl.bitlinear_forward(xq[(M, p.K)], sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
+                                         y=ys[(M, p.N)], workspace=fwd_ws[(M, p.N, p.K)])
+                    if ev is not None:
+                        ev[i][1].record(stream)
+                    i += 1
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    # ---- warmup: W steps, then more untimed steps until ~1 s has passed (clock ramp-up)
+    t0 = time.perf_counter()
+    n = 0
+    while n < args.warmup or time.perf_counter() - t0 < 1.0:
+        step()
+        n += 1
+        if n % 20 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, per-launch events on the forward kernels
+    per_step_launches = len(alg_bytes_fwd)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(per_step_launches)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = bl.bitlinear_kernel_launches()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = bl.bitlinear_kernel_launches() - launches0
+    ms = start.elapsed_time(end) / args.steps
+    fwd_ms = [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps
+              for i in range(per_step_launches)]
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * packed_bytes_step / (ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API: pinned host inputs in, bf16 outputs out
+    host_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
+    host_y = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in ys.items()}
+    dev_x = {k: torch.empty_like(v) for k, v in xs.items()}
+    h2d = d2h = 0
+    for M in wl.tokens:
+        for row in weights:
+            for (p, _, _) in row:
+                h2d += M * p.K * 2
+                d2h += M * p.N * 2
+
+    def e2e_step():
+        for M in wl.tokens:
+            for row in weights:
+                for (p, packed, w_scale) in row:
+                    dev_x[(M, p.K)].copy_(host_x[(M, p.K)], non_blocking=True)
+                    q, s_ = bl.bitlinear_quant_act(dev_x[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)],
+                                                   act_scale=sc[(M, p.K)])
+                    y = bl.bitlinear_forward(q, s_, packed, w_scale, out_dtype=torch.bfloat16, y=ys[(M, p.N)],
+                                             workspace=fwd_ws[(M, p.N, p.K)])
+                    host_y[(M, p.N)].copy_(y, non_blocking=True)
+
+    for _ in range(max(args.warmup, 1)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * packed_bytes_step / (e2e_ms * 1e-3) / 1e9
+
+    # ---- roofline of the dominant kernel (the contraction)
+    hbm, bf16_tf, peak_src = measured_peaks()
+    achieved = sum(alg_bytes_fwd) / (sum(fwd_ms) * 1e-3) / 1e9
+    traffic = traffic_record(os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc", "gemv.cu"))
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic, "peak_source": peak_src,
+                "kernel": "bitlinear_forward (ternary contraction + dequant)",
+                "alg_bytes_per_launch": sum(alg_bytes_fwd) / len(alg_bytes_fwd),
+                "avg_launch_us": sum(fwd_ms) / len(fwd_ms) * 1e3,
+                "share_of_step": sum(fwd_ms) / ms if ms > 0 else None}
+
+    # ---- CPU baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, el, reps = oracle_sample(args.ref_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"layer 0 of {LAYERS} (QKV, O, gate+up, down) at M=1 and M=8, {reps} passes in {el:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic (seeded N(0,0.02) latent weights, N(0,1) bf16 activations)",
+        "config": {"workload": WORKLOAD, "layers": layers, "tokens": list(wl.tokens),
+                   "projections": [[p.name, p.K, p.N] for p in wl.projections],
+                   "packed_bytes_per_step": packed_bytes_step,
+                   "l2": "no flush: 520 MB of distinct packed weights per pass (> 4x the 126 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--ref-seconds", type=float, default=12.0, help="CPU oracle seconds per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return our_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

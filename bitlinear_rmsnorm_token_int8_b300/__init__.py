@@ -1,1 +1,185 @@
-"""BitNet b1.58 BitLinear forward on B300 (sm_103a): placeholder, binding added next."""
+"""BitNet b1.58 BitLinear forward on one B300 GPU (sm_103a).
+
+Thin Python binding over the C ABI of ``libbitlinear.so`` (declared in
+``include/bitlinear.h``).  Every function here only marshals arguments: it
+allocates outputs with PyTorch when the caller gives none, passes raw device
+pointers and the current CUDA stream, and turns a non-OK status into
+:class:`BitLinearError`.  All arithmetic runs in the library's CUDA kernels;
+there is no CPU fallback, and every call fails loudly if the library is missing.
+
+Steps (page "BitNet b1.58 in Production: 1-Bit LLMs and Energy Benchmarks",
+section "The Mathematical Mechanism", items 1-4):
+
+* :func:`bitlinear_pack_weights`  absmean ternarization + 2-bit packing
+* :func:`bitlinear_quant_act`     RMSNorm + per-token absmax int8 quantization
+* :func:`bitlinear_forward`       exact int32 ternary contraction + dequantization
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "BitLinearError", "lib", "library_path", "bitlinear_pack_weights", "bitlinear_quant_act",
+    "bitlinear_forward", "bitlinear_get_device_error", "bitlinear_packed_bytes",
+    "bitlinear_forward_workspace_bytes", "bitlinear_pack_workspace_bytes", "OUT_F32", "OUT_BF16",
+    "STATUS", "bitlinear_kernel_launches",
+]
+
+OUT_F32 = 0
+OUT_BF16 = 1
+STATUS = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_DTYPE", 5: "ERR_DEVICE",
+          6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_WORKSPACE", 9: "ERR_NONFINITE"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libbitlinear.so")
+_lib = None
+
+
+class BitLinearError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({message})")
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(
+                f"{library_path} is missing: build it with "
+                "`python -m bitlinear_rmsnorm_token_int8_b300.build` (no CPU fallback exists)")
+        L = ctypes.CDLL(library_path)
+        P, I64, SZ, F, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_int
+        L.bitlinear_status_string.argtypes = [I]
+        L.bitlinear_status_string.restype = ctypes.c_char_p
+        L.bitlinear_abi_version.restype = I
+        L.bitlinear_kernel_launches.restype = ctypes.c_uint64
+        L.bitlinear_packed_bytes.argtypes = [I64, I64]
+        L.bitlinear_packed_bytes.restype = SZ
+        L.bitlinear_pack_workspace_bytes.argtypes = [I64, I64]
+        L.bitlinear_pack_workspace_bytes.restype = SZ
+        L.bitlinear_pack_weights.argtypes = [P, I64, I64, F, P, P, P, P, SZ, P]
+        L.bitlinear_pack_weights.restype = I
+        L.bitlinear_quant_act.argtypes = [P, P, F, I64, I64, P, P, P]
+        L.bitlinear_quant_act.restype = I
+        L.bitlinear_forward_workspace_bytes.argtypes = [I64, I64, I64]
+        L.bitlinear_forward_workspace_bytes.restype = SZ
+        L.bitlinear_forward.argtypes = [P, P, P, P, I64, I64, I64, I, P, P, P, SZ, P]
+        L.bitlinear_forward.restype = I
+        L.bitlinear_get_device_error.argtypes = [P]
+        L.bitlinear_get_device_error.restype = I
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise BitLinearError(fn, status, lib().bitlinear_status_string(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def bitlinear_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().bitlinear_kernel_launches())
+
+
+def bitlinear_packed_bytes(N: int, K: int) -> int:
+    return int(lib().bitlinear_packed_bytes(N, K))
+
+
+def bitlinear_pack_workspace_bytes(N: int, K: int) -> int:
+    return int(lib().bitlinear_pack_workspace_bytes(N, K))
+
+
+def bitlinear_forward_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().bitlinear_forward_workspace_bytes(M, N, K))
+
+
+def bitlinear_pack_weights(W: torch.Tensor, eps: float = 1e-5, packed=None, w_scale=None,
+                           gamma=None, workspace=None, stream=None):
+    """Ternarize + pack latent weights W [N,K] fp32 (CUDA).  Returns (packed, w_scale, gamma)."""
+    _cuda(W, "W", torch.float32)
+    N, K = W.shape
+    dev = W.device
+    if packed is None:
+        packed = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+    if w_scale is None:
+        w_scale = torch.empty(N, dtype=torch.float32, device=dev)
+    if gamma is None:
+        gamma = torch.empty(4, dtype=torch.float32, device=dev)[:1]
+    if workspace is None:
+        workspace = torch.empty(bitlinear_pack_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    _check("bitlinear_pack_weights", lib().bitlinear_pack_weights(
+        _ptr(W), N, K, float(eps), _ptr(packed), _ptr(w_scale), _ptr(gamma), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return packed, w_scale, gamma
+
+
+def bitlinear_quant_act(x: torch.Tensor, gain=None, rms_eps: float = 1e-5, x_q=None,
+                        act_scale=None, stream=None):
+    """RMSNorm + per-token int8 quantization of x [M,K] bf16 (CUDA).  Returns (x_q, act_scale).
+
+    ``rms_eps < 0`` skips RMSNorm; ``gain`` is the RMSNorm weight (bf16 [K]) or None.
+    """
+    _cuda(x, "x", torch.bfloat16)
+    M, K = x.shape
+    if gain is not None:
+        _cuda(gain, "gain", torch.bfloat16)
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if act_scale is None:
+        act_scale = torch.empty(max(M, 1) + 3, dtype=torch.float32, device=x.device)[:M]
+    _check("bitlinear_quant_act", lib().bitlinear_quant_act(
+        _ptr(x), _ptr(gain), float(rms_eps), M, K, _ptr(x_q), _ptr(act_scale), _stream(stream)))
+    return x_q, act_scale
+
+
+def bitlinear_forward(x_q: torch.Tensor, act_scale: torch.Tensor, packed: torch.Tensor,
+                      w_scale: torch.Tensor, out_dtype=torch.bfloat16, y=None, acc_debug=None,
+                      workspace=None, stream=None):
+    """y [M,N] = dequant(x_q . W_q^T) (CUDA).  ``acc_debug``: optional int32 [M,N] out."""
+    _cuda(x_q, "x_q", torch.int8)
+    _cuda(packed, "packed", torch.uint8)
+    M, K = x_q.shape
+    N = packed.shape[0]
+    code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(out_dtype)
+    if code is None:
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x_q.device)
+    need = bitlinear_forward_workspace_bytes(M, N, K)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x_q.device)
+    _check("bitlinear_forward", lib().bitlinear_forward(
+        _ptr(x_q), _ptr(act_scale), _ptr(packed), _ptr(w_scale), M, N, K, code, _ptr(y),
+        _ptr(acc_debug), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _stream(stream)))
+    return y
+
+
+def bitlinear_get_device_error(stream=None) -> int:
+    """Waits for the stream; returns and clears the device error word (0 = none)."""
+    return int(lib().bitlinear_get_device_error(_stream(stream)))

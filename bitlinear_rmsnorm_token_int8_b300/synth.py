@@ -112,3 +112,10 @@ def act_seed(workload_seed: int, M: int, K: int) -> int:
 
 def gain_seed(workload_seed: int, layer: int, which: int) -> int:
     return workload_seed * 50021 + layer * 11 + which
+
+
+def latent_weights_device(N: int, K: int, seed: int, device, std: float = WEIGHT_STD) -> torch.Tensor:
+    """Same distribution as :func:`latent_weights`, drawn on ``device`` (for large benchmark
+    stacks; the values differ from the CPU draw, the distribution does not)."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    return torch.randn(N, K, generator=g, dtype=torch.float32, device=device) * std

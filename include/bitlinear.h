@@ -1,0 +1,187 @@
+/*
+ * bitlinear.h - C ABI of the BitNet b1.58 BitLinear forward for one B300 GPU (sm_103a).
+ *
+ * The forward has three steps, each an entry point below:
+ *   1. bitlinear_pack_weights: absmean ternarization of the latent weights and
+ *      2-bit packing (done once per weight matrix);
+ *   2. bitlinear_quant_act: RMSNorm + per-token absmax int8 quantization of the
+ *      activations;
+ *   3. bitlinear_forward: exact int32 ternary contraction of the int8 tokens with
+ *      the packed weights, dequantized by gamma * max|x| / 127.
+ *
+ * Sources (page title, section):
+ *   [P4-eq]   "BitNet b1.58 in Production: 1-Bit LLMs and Energy Benchmarks",
+ *             "The Mathematical Mechanism: BitLinear vs Standard Linear", items 1-4.
+ *   [P4-code] same page, "Production Multi-File Implementation", bit_linear.py
+ *             (weight_quant, activation_quant, BitLinear.forward).
+ *   [P5-lut]  "BitNet 1-bit LLM Inference Framework", "How the LUT Kernel Works"
+ *             (2-bit code 00 = 0, 01 = +1, 10 = -1, four weights per byte;
+ *             int32 accumulation, C signature (act, weight, out, M, N, K)).
+ *   [P1-impl] "BitNet's 1-Bit Transformer: Architecture Breakdown", "Core
+ *             Modifications", item 1 (bitlinear_forward(x, W_packed, s)).
+ *
+ * Conventions shared by every call:
+ *   - Pointers are DEVICE pointers owned by the caller (allocated e.g. by PyTorch),
+ *     16-byte aligned, row-major and densely packed.  The library allocates, frees
+ *     and synchronizes nothing inside these calls; scratch memory is the caller's
+ *     `workspace`, sized by the matching *_workspace_bytes function.
+ *   - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream).  Results are valid once the stream has reached them.
+ *   - Argument errors are reported synchronously before anything is enqueued, and
+ *     then nothing is written.  A failed launch returns BITLINEAR_ERR_CUDA.  Errors
+ *     found on the device (a non-finite weight, a bounded wait that ran out) are
+ *     recorded in a per-device error word read by bitlinear_get_device_error.
+ *   - The calling thread's current CUDA device must be an sm_103 GPU (B300), else
+ *     BITLINEAR_ERR_DEVICE.  No exception crosses the ABI.
+ */
+#ifndef BITLINEAR_H_
+#define BITLINEAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bitlinear_status {
+    BITLINEAR_OK = 0,
+    BITLINEAR_ERR_NULL = 1,       /* a required pointer is NULL */
+    BITLINEAR_ERR_SHAPE = 2,      /* a size is negative, zero where it must not be, or breaks a divisibility rule */
+    BITLINEAR_ERR_ALIGN = 3,      /* a pointer is not 16-byte aligned */
+    BITLINEAR_ERR_DTYPE = 4,      /* unknown out_dtype */
+    BITLINEAR_ERR_DEVICE = 5,     /* current device is not sm_103, or no device */
+    BITLINEAR_ERR_CUDA = 6,       /* a CUDA runtime call or launch failed */
+    BITLINEAR_ERR_TIMEOUT = 7,    /* device: a bounded wait in a kernel ran out */
+    BITLINEAR_ERR_WORKSPACE = 8,  /* workspace missing or smaller than required */
+    BITLINEAR_ERR_NONFINITE = 9   /* device: a latent weight was Inf or NaN */
+} bitlinear_status;
+
+/* Output element types of bitlinear_forward. */
+#define BITLINEAR_OUT_F32 0
+#define BITLINEAR_OUT_BF16 1
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *bitlinear_status_string(bitlinear_status status);
+
+/* ABI version, currently 1. */
+int bitlinear_abi_version(void);
+
+/* Number of kernels this library has enqueued in this process so far (all devices,
+ * all threads; memsets not counted).  For accounting in benchmarks and tests. */
+uint64_t bitlinear_kernel_launches(void);
+
+/* ------------------------------------------------------------------------ */
+/* 1. weights                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of the packed ternary matrix: N * K / 4. */
+size_t bitlinear_packed_bytes(int64_t N, int64_t K);
+
+/* Bytes of scratch that bitlinear_pack_weights needs (independent of N and K). */
+size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K);
+
+/*
+ * Absmean ternarization and 2-bit packing of one latent weight matrix
+ * ([P4-eq] item 1; [P4-code] weight_quant; [P5-lut] code table).
+ *
+ *   gamma  = (1/(N K)) sum |W|, the exact mean rounded once to binary32
+ *   d      = fl32(gamma + eps)
+ *   W_q    = Clip(Round(W / d), -1, 1)   (Round: nearest, ties to even)
+ *
+ * W        [N,K] fp32, nn.Linear layout (row n = output feature n).  Must be finite.
+ * N, K     N >= 1, K >= 4, K % 4 == 0, N*K < 2^32.
+ * eps      the eps of the divisor (1e-5 in BitNet b1.58); must be >= 0.
+ * packed   [N, K/4] uint8 out: weight k of row n in byte n*K/4 + k/4, bits
+ *          2*(k%4)..2*(k%4)+1, code 00 = 0, 01 = +1, 10 = -1 (11 never written).
+ * w_scale  [N] fp32 out: gamma repeated for every row (a per-row scale vector lets
+ *          several matrices be stacked into one fused projection).
+ * gamma_out [1] fp32 out, or NULL.
+ * workspace >= bitlinear_pack_workspace_bytes(N,K) bytes of device scratch; its
+ *          contents on entry do not matter (the call clears what it uses).
+ * Device errors: a non-finite weight sets BITLINEAR_ERR_NONFINITE in the device
+ *          error word; the outputs are then unspecified.
+ */
+bitlinear_status bitlinear_pack_weights(const float *W, int64_t N, int64_t K, float eps,
+                                        uint8_t *packed, float *w_scale, float *gamma_out,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* 2. activations                                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * RMSNorm + per-token absmax int8 quantization ([P4-code] BitLinear.forward
+ * steps 1-2 and activation_quant; [P4-eq] item 2, Q_b = 127), one token per row:
+ *
+ *   n_k    = x_k * r * g_k,  r = 1/sqrt(mean_k x_k^2 + rms_eps)      (RMSNorm)
+ *   x_q[k] = Clip(Round(127 * n_k / max_k|n_k|), -128, 127)          (Round: ties to even)
+ *   act_scale = max_k|n_k| / 127                                      (sigma, the per-token dequant factor)
+ *
+ * Because r > 0 is one number per row, x_q equals the codes of x*g computed
+ * exactly: the kernel decides every code from exact binary32 products, so x_q is
+ * bit-exact whatever the summation order of mean(x^2).  A row whose max|x*g| is
+ * below 1e-8 uses 1e-8 as its max (all-zero rows give zero codes).
+ *
+ * x_bf16   [M,K] bf16 tokens.  Must be finite, with |x| <= 2^60 and |x*g| <= 2^100
+ *          (beyond that the fp32 squares or products may overflow).
+ * gain_bf16 [K] bf16 RMSNorm weight g, or NULL for g = 1.
+ * rms_eps  eps of RMSNorm (>= 0); a negative value disables RMSNorm (r = 1).
+ * M, K     M >= 0 (M == 0 enqueues nothing and accepts NULL buffers), 8 <= K <= 65536,
+ *          K % 8 == 0.
+ * x_q      [M,K] int8 out.  act_scale [M] fp32 out.
+ */
+bitlinear_status bitlinear_quant_act(const void *x_bf16, const void *gain_bf16, float rms_eps,
+                                     int64_t M, int64_t K, int8_t *x_q, float *act_scale,
+                                     void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* 3. ternary contraction + dequantization                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of scratch that bitlinear_forward needs for this shape (may be 0). */
+size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * y = dequant(x_q . W_q^T) ([P4-eq] items 3-4; [P5-lut] accumulation loop;
+ * [P1-impl] bitlinear_forward(x, W_packed, s)):
+ *
+ *   acc[t][n] = sum_k W_q[n][k] * x_q[t][k]                 exact, int32
+ *   y[t][n]   = fl32(fl32(acc * act_scale[t]) * w_scale[n]) then, for bf16
+ *               output, rounded to nearest even bf16.
+ *
+ * x_q       [M,K] int8 (from bitlinear_quant_act).  Codes must lie in [-127,127].
+ * act_scale [M] fp32.   packed [N,K/4] uint8 (from bitlinear_pack_weights).
+ * w_scale   [N] fp32.
+ * M, N, K   0 <= M <= 2^24 (M == 0 enqueues nothing and accepts NULL buffers),
+ *           16 <= N <= 2^24, N % 16 == 0, 128 <= K <= 65536, K % 128 == 0.
+ * out_dtype BITLINEAR_OUT_F32 or BITLINEAR_OUT_BF16.
+ * y         [M,N] out, fp32 or bf16.
+ * acc_debug [M,N] int32 out with the raw accumulators, or NULL (for parity checks).
+ * workspace >= bitlinear_forward_workspace_bytes(M,N,K) bytes of device scratch
+ *           (may be NULL when that is 0).  Contents on entry do not matter.
+ */
+bitlinear_status bitlinear_forward(const int8_t *x_q, const float *act_scale,
+                                   const uint8_t *packed, const float *w_scale,
+                                   int64_t M, int64_t N, int64_t K, int out_dtype, void *y,
+                                   int32_t *acc_debug, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* device error word                                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Waits for `stream`, then returns and clears the current device's error word:
+ * BITLINEAR_OK if no kernel of this library recorded an error since the last
+ * call, else the first recorded device status (BITLINEAR_ERR_TIMEOUT,
+ * BITLINEAR_ERR_NONFINITE).  Returns BITLINEAR_ERR_CUDA if the wait or the read
+ * fails.  This is the only call that synchronizes.
+ */
+bitlinear_status bitlinear_get_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITLINEAR_H_ */

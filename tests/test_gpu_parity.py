@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars (derivations in DESIGN.md, "Tolerances"):
+* int8 codes, packed bytes, gamma and int32 accumulators: bit-exact;
+* act_scale (sigma): relative error <= 5e-7 against the oracle's fp64 value;
+* fp32 output: relative error <= 1e-6 against the oracle's fp64 output;
+* bf16 output: within 1 bf16 ulp of the oracle's fp64 output rounded to bf16.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bitlinear_rmsnorm_token_int8_b300 as bl
+import oracle
+from bitlinear_rmsnorm_token_int8_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+RMS_EPS = float(np.float32(1e-5))
+SIGMA_RTOL = 5e-7
+F32_RTOL = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    bl.lib()
+    yield
+    assert bl.bitlinear_get_device_error() == 0
+
+
+def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    def ordered(u):
+        u = u.astype(np.int32)
+        return np.where(u & 0x8000, -(u & 0x7FFF), u & 0x7FFF)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def f64_to_bf16_bits(y: np.ndarray) -> np.ndarray:
+    # round the fp64 value to fp32 then bf16; the double rounding can differ from a
+    # direct fp64 -> bf16 rounding only at exact bf16 ties, within the 1-ulp bar
+    return oracle.f32_to_bf16_bits(y.astype(np.float32))
+
+
+def gpu_quant(x_bf16: torch.Tensor, gain, rms_eps):
+    xq, sc = bl.bitlinear_quant_act(x_bf16.cuda(), None if gain is None else gain.cuda(), rms_eps)
+    torch.cuda.synchronize()
+    return xq.cpu().numpy(), sc.cpu().numpy().astype(np.float64)
+
+
+def gpu_pack(W: torch.Tensor, eps=1e-5):
+    packed, ws, gamma = bl.bitlinear_pack_weights(W.cuda(), eps)
+    torch.cuda.synchronize()
+    return packed.cpu().numpy(), ws.cpu().numpy(), np.float32(gamma.cpu().item())
+
+
+# ---------------------------------------------------------------------------
+# activation quantization
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,gain,rms,outliers", [
+    (1, 8, False, True, False), (3, 256, True, True, True), (17, 2560, True, True, True),
+    (5, 6912, False, True, True), (4, 14336, True, True, False), (2, 16392, True, True, True),
+    (2, 65536, True, True, True), (33, 4096, True, False, True), (64, 1024, False, False, False),
+])
+def test_quant_act_matches_oracle(M, K, gain, rms, outliers):
+    x = synth.activations(M, K, seed=10 * M + K, outliers=outliers)
+    g = synth.rms_gains(K, seed=K) if gain else None
+    eps = RMS_EPS if rms else -1.0
+    xq, sc = gpu_quant(x, g, eps)
+    oq, osig = oracle.act_quant(synth.bf16_bits(x), None if g is None else synth.bf16_bits(g), eps)
+    assert (xq == oq).all()
+    assert np.all(np.abs(sc - osig) <= SIGMA_RTOL * osig)
+
+
+def test_quant_act_edge_rows():
+    K = 512
+    rows = np.zeros((6, K), dtype=np.float32)
+    rows[1, 0] = 127.0                         # ties: 127 * x / 127 = x
+    rows[1, 1:9] = [2.5, 1.5, 0.5, -0.5, -1.5, -2.5, 3.5, -3.5]
+    rows[2, :] = 1e-12                         # max below the 1e-8 guard
+    rows[2, 7] = -3e-12
+    rows[3, :] = -7.0                          # constant row
+    rng = np.random.default_rng(0)
+    rows[4] = rng.integers(-254, 255, K) / 2.0  # many half-integer ties after scaling
+    rows[4, 3] = 127.0
+    rows[5] = rng.standard_normal(K) * 1e15     # large magnitudes (|x| <= 2^60 contract)
+    bits = oracle.f32_to_bf16_bits(rows)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    for gain in (None, synth.rms_gains(K, seed=3)):
+        xq, sc = gpu_quant(x, gain, RMS_EPS)
+        oq, osig = oracle.act_quant(bits, None if gain is None else synth.bf16_bits(gain), RMS_EPS)
+        assert (xq == oq).all()
+        assert np.all(np.abs(sc - osig) <= SIGMA_RTOL * osig)
+    assert (xq[0] == 0).all()
+
+
+def test_quant_act_empty_is_noop():
+    x = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    xq, sc = bl.bitlinear_quant_act(x)
+    assert xq.shape == (0, 256) and sc.shape == (0,)
+
+
+# ---------------------------------------------------------------------------
+# weight packing
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(1, 4), (3, 20), (16, 256), (512, 256), (37, 2560), (2560, 6912)])
+def test_pack_matches_oracle(N, K):
+    W = synth.latent_weights(N, K, seed=N * 7 + K)
+    packed, ws, gamma = gpu_pack(W)
+    o_packed, o_gamma, _ = oracle.pack_weights(W.numpy())
+    assert gamma == o_gamma
+    assert (ws == o_gamma).all()
+    assert (packed == o_packed).all()
+
+
+def test_pack_adversarial_values():
+    rng = np.random.default_rng(1)
+    N, K = 24, 64
+    W = (rng.standard_normal((N, K)) * np.exp2(rng.integers(-140, 60, (N, K)))).astype(np.float32)
+    W[0, :8] = [1.4e-45, -1.4e-45, 1e-40, -0.0, 0.0, 3e38, -3e38, 1.0]
+    for Wt in (W, np.abs(W), np.full((N, K), 2.0**-149, dtype=np.float32)):
+        packed, ws, gamma = gpu_pack(torch.from_numpy(np.ascontiguousarray(Wt)))
+        o_packed, o_gamma, _ = oracle.pack_weights(Wt)
+        assert gamma == o_gamma, (gamma, o_gamma)
+        assert (packed == o_packed).all()
+
+
+def test_pack_gamma_ties_round_to_even():
+    # mean = 1 + 2^-24 exactly: halfway between 1 and 1 + 2^-23 -> 1 (even)
+    # mean = 1 + 3*2^-24: halfway between 1 + 2^-23 (odd) and 1 + 2^-22 -> 1 + 2^-22
+    one_up = np.float32(1 + 2.0**-23)
+    for w, expect in (([1.0, one_up, 1.0, one_up], np.float32(1.0)),
+                      ([one_up, np.float32(1 + 2.0**-22), one_up, np.float32(1 + 2.0**-22)],
+                       np.float32(1 + 2.0**-22))):
+        Wt = torch.tensor([w], dtype=torch.float32)
+        _, _, gamma = gpu_pack(Wt)
+        assert gamma == expect == oracle.absmean_gamma(Wt.numpy())
+
+
+def test_pack_threshold_ties():
+    # weights exactly at d/2 (a tie, rounds to 0) and one binary32 step above (rounds to 1)
+    rng = np.random.default_rng(2)
+    W = (rng.standard_normal((8, 64)) * 0.02).astype(np.float32)
+    g = oracle.absmean_gamma(W)
+    d = np.float32(g + np.float32(1e-5))
+    half = np.float32(d / np.float32(2))
+    # small edits that keep the absmean unchanged are hard; instead check codes with the
+    # oracle on the full matrix including elements placed near the threshold
+    W[0, :4] = [half, -half, np.nextafter(half, np.float32(1)), -np.nextafter(half, np.float32(1))]
+    packed, _, gamma = gpu_pack(torch.from_numpy(W))
+    o_packed, o_gamma, q = oracle.pack_weights(W)
+    assert gamma == o_gamma and (packed == o_packed).all()
+
+
+def test_pack_nonfinite_sets_device_error():
+    W = torch.zeros((4, 16), dtype=torch.float32)
+    W[1, 3] = float("inf")
+    bl.bitlinear_pack_weights(W.cuda())
+    assert bl.bitlinear_get_device_error() == 9
+    assert bl.bitlinear_get_device_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# contraction + dequantization
+# ---------------------------------------------------------------------------
+
+def run_forward(M, N, K, out_dtype, seed, outliers=True, gain=True):
+    x = synth.activations(M, K, seed=seed, outliers=outliers)
+    g = synth.rms_gains(K, seed=seed + 1) if gain else None
+    W = synth.latent_weights(N, K, seed=seed + 2)
+    packed, w_scale, gamma = bl.bitlinear_pack_weights(W.cuda())
+    xq, sc = bl.bitlinear_quant_act(x.cuda(), None if g is None else g.cuda(), RMS_EPS)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = bl.bitlinear_forward(xq, sc, packed, w_scale, out_dtype=out_dtype, acc_debug=acc)
+    torch.cuda.synchronize()
+    o_xq, o_sig = oracle.act_quant(synth.bf16_bits(x), None if g is None else synth.bf16_bits(g), RMS_EPS)
+    o_packed, o_gamma, o_wq = oracle.pack_weights(W.numpy())
+    return dict(x=x, y=y.cpu(), acc=acc.cpu().numpy(), xq=xq.cpu().numpy(), sc=sc.cpu().numpy(),
+                packed=packed.cpu().numpy(), gamma=np.float32(gamma.cpu().item()),
+                o_xq=o_xq, o_sig=o_sig, o_packed=o_packed, o_gamma=o_gamma, o_wq=o_wq)
+
+
+def check_output(r, ts=None, ns=None):
+    """acc bit-exact; y against the oracle's fp64 y (all, or at (ts, ns))."""
+    assert (r["xq"] == r["o_xq"]).all()
+    assert (r["packed"] == r["o_packed"]).all() and r["gamma"] == r["o_gamma"]
+    if ts is None:
+        o_acc = oracle.ternary_matmul(r["o_xq"], r["o_wq"])
+        assert (r["acc"] == o_acc).all()
+        N = o_acc.shape[1]
+        o_y = oracle.dequant(o_acc, r["o_sig"], np.full(N, float(r["o_gamma"])))
+        gy = r["y"]
+    else:
+        o_acc = oracle.ternary_matmul_at(r["o_xq"], r["o_wq"], ts, ns)
+        assert (r["acc"][ts, ns] == o_acc).all()
+        o_y = o_acc.astype(np.float64) * r["o_sig"][ts] * float(r["o_gamma"])
+        gy = r["y"][ts, ns]
+    if gy.dtype == torch.float32:
+        g = gy.numpy().astype(np.float64)
+        assert np.all(np.abs(g - o_y) <= F32_RTOL * np.abs(o_y))
+    else:
+        gb = gy.view(torch.int16).numpy().view(np.uint16)
+        assert bf16_ulp_distance(gb, f64_to_bf16_bits(o_y)).max() <= 1
+
+
+@pytest.mark.parametrize("M,N,K,dt", [
+    (4, 512, 256, torch.float32),        # the single-layer K=256 -> N=512, 4-token case
+    (1, 16, 128, torch.float32), (3, 48, 384, torch.bfloat16), (8, 272, 640, torch.float32),
+    (17, 160, 1024, torch.bfloat16), (16, 2560, 2560, torch.float32), (40, 256, 6912, torch.bfloat16),
+    (129, 384, 512, torch.float32),
+])
+def test_forward_matches_oracle(M, N, K, dt):
+    r = run_forward(M, N, K, dt, seed=M * 131 + N + K)
+    check_output(r)
+
+
+def test_forward_teacher_forced_dequant_is_two_roundings():
+    # y = fl(fl(acc * sigma) * w_scale): with the GPU's own sigma and gamma the fp64
+    # product differs from the fp32 output by at most two binary32 roundings
+    r = run_forward(8, 512, 1024, torch.float32, seed=5)
+    y64 = r["acc"].astype(np.float64) * r["sc"].astype(np.float64)[:, None] * float(r["gamma"])
+    y32 = r["y"].numpy().astype(np.float64)
+    assert np.all(np.abs(y32 - y64) <= 2.0**-23 * np.abs(y64))
+    # and it is exactly that pair of fp32 products
+    a = r["acc"].astype(np.float32) * r["sc"][:, None]
+    assert (a.astype(np.float32) * r["gamma"] == r["y"].numpy()).all()
+
+
+def test_forward_weight_invariants_on_gpu():
+    # all +1 rows -> row sums of x_q; all -1 -> their negation; all 0 -> 0
+    M, K = 5, 512
+    xq = torch.randint(-127, 128, (M, K), dtype=torch.int8)
+    sc = torch.ones(M, dtype=torch.float32)
+    for code, sign in ((0x55, 1), (0xAA, -1), (0x00, 0)):
+        packed = torch.full((32, K // 4), code, dtype=torch.uint8)
+        acc = torch.empty((M, 32), dtype=torch.int32, device="cuda")
+        bl.bitlinear_forward(xq.cuda(), sc.cuda(), packed.cuda(), torch.ones(32).cuda(),
+                             out_dtype=torch.float32, acc_debug=acc)
+        expect = sign * xq.to(torch.int64).sum(dim=1)
+        assert (acc.cpu().to(torch.int64) == expect[:, None]).all()
+
+
+def test_forward_extreme_codes_max_k():
+    # |acc| reaches 127 * K at the largest K: exactness of the int32 path
+    M, N, K = 2, 32, 65536
+    xq = torch.full((M, K), 127, dtype=torch.int8)
+    xq[1] = -127
+    packed = torch.full((N, K // 4), 0x55, dtype=torch.uint8)
+    packed[1::2] = 0xAA
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    bl.bitlinear_forward(xq.cuda(), torch.ones(M).cuda(), packed.cuda(), torch.ones(N).cuda(),
+                         out_dtype=torch.float32, acc_debug=acc)
+    a = acc.cpu()
+    assert a[0, 0] == 127 * K and a[0, 1] == -127 * K and a[1, 0] == -127 * K
+
+
+def test_forward_empty_is_noop():
+    packed = torch.zeros((16, 32), dtype=torch.uint8, device="cuda")
+    y = bl.bitlinear_forward(torch.zeros((0, 128), dtype=torch.int8, device="cuda"),
+                             torch.zeros(0, device="cuda"), packed, torch.ones(16, device="cuda"))
+    assert y.shape == (0, 16)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled outputs, full x_q / packed comparison
+# ---------------------------------------------------------------------------
+
+FULL = []
+for wl_name in ("decode_2b", "decode_8b", "prefill_8b_m2048"):
+    wl = synth.WORKLOADS[wl_name]
+    for M in wl.tokens:
+        for pi, p in enumerate(wl.projections):
+            FULL.append((wl_name, M, pi))
+
+
+@pytest.mark.parametrize("wl_name,M,pi", FULL)
+def test_full_size_sampled(wl_name, M, pi):
+    wl = synth.WORKLOADS[wl_name]
+    p = wl.projections[pi]
+    dt = torch.float32 if wl.out_dtype == "f32" else torch.bfloat16
+    r = run_forward(M, p.N, p.K, dt, seed=synth.weight_seed(wl.seed, 0, pi), outliers=wl.outliers)
+    rng = np.random.default_rng(pi + M)
+    ts = rng.integers(0, M, 512)
+    ns = rng.integers(0, p.N, 512)
+    ts[:2] = [0, M - 1]
+    ns[:2] = [0, p.N - 1]
+    check_output(r, ts, ns)
