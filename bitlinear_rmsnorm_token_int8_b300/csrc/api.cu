@@ -70,6 +70,11 @@ static std::atomic<uint64_t> g_launches{0};
 
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+int* current_device_error_word() {
+  const DeviceState* s = current_device();
+  return s ? s->err_word : nullptr;
+}
+
 int num_sms() {
   const DeviceState* s = current_device();
   return s ? s->sms : 148;

@@ -37,6 +37,10 @@ cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint
 
 int num_sms();
 
+// Checks that the calling thread's current device is usable (sm_103) and returns
+// the device address of its error word, or nullptr.
+int* current_device_error_word();
+
 // Adds n to the process-wide count of kernels enqueued by this library.
 void count_launches(int n);
 

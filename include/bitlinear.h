@@ -106,6 +106,29 @@ bitlinear_status bitlinear_pack_weights(const float *W, int64_t N, int64_t K, fl
                                         uint8_t *packed, float *w_scale, float *gamma_out,
                                         void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * bitlinear_pack_weights without a workspace argument: the same kernels and the
+ * same results, with the ~2 KB of scratch taken from a fixed array that the
+ * library keeps in each GPU's memory.  The pages have no counterpart to this
+ * call; it is here for callers that cannot allocate device memory, such as a
+ * plugin that is only handed buffers its host framework sized in advance, or
+ * code on a latency-critical path where cudaMalloc/cudaFree may synchronize the
+ * device or fail under memory pressure.  The call itself allocates nothing.
+ *
+ * Arguments, layouts and device errors: as bitlinear_pack_weights.
+ * Limit: N*K < 2^32 (else BITLINEAR_ERR_SHAPE); the fixed scratch holds
+ *   bitlinear_pack_workspace_bytes() bytes, which covers every size within it.
+ * The first call on each device looks up the array's device address with that
+ *   device current, so make it before any stream capture.
+ * Every GPU that loads the library holds the array until the process exits.
+ * All calls on a device share the one array and leave their contents in it;
+ *   each call clears what it accumulates into, but calls whose work overlaps on
+ *   the GPU (unordered streams) race on it: order them.
+ */
+bitlinear_status bitlinear_pack_weights_static(const float *W, int64_t N, int64_t K, float eps,
+                                               uint8_t *packed, float *w_scale, float *gamma_out,
+                                               void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* 2. activations                                                            */
 /* ------------------------------------------------------------------------ */
