@@ -279,7 +279,7 @@ def our_arm(args):
 
     # ---- activations and buffers
     Ks = sorted({p.K for p in wl.projections})
-    xs, gains, xq, sc, ys = {}, {}, {}, {}, {}
+    xs, gains, xq, sc, ops, ys = {}, {}, {}, {}, {}, {}
     for K in Ks:
         gains[K] = synth.rms_gains(K, synth.gain_seed(wl.seed, 0, K)).to(dev)
     for M in wl.tokens:
@@ -287,33 +287,36 @@ def our_arm(args):
             xs[(M, K)] = synth.activations(M, K, synth.act_seed(wl.seed, M, K), outliers=False).to(dev)
             xq[(M, K)] = torch.empty((M, K), dtype=torch.int8, device=dev)
             sc[(M, K)] = torch.empty(M + 4, dtype=torch.float32, device=dev)[:M]
+            ops[(M, K)] = torch.empty(bl.bitlinear_act_ops_bytes(M, K), dtype=torch.uint8, device=dev)
         for p in wl.projections:
             ys[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
-    fwd_ws = {}
-    for M in wl.tokens:
-        for p in wl.projections:
-            need = bl.bitlinear_forward_workspace_bytes(M, p.N, p.K)
-            fwd_ws[(M, p.N, p.K)] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
 
     packed_bytes_step = sum(p.N * p.K // 4 for _ in wl.tokens for row in weights for (p, _, _) in row)
     alg_bytes_fwd = []     # algorithmic bytes of each forward launch, in launch order
     for M in wl.tokens:
         for row in weights:
             for (p, _, _) in row:
-                alg_bytes_fwd.append(p.N * p.K // 4 + M * p.K + 4 * M + 4 * p.N + 2 * M * p.N)
+                alg_bytes_fwd.append(p.N * p.K // 4 + 2 * M * p.K + 4 * M + 4 * p.N + 2 * M * p.N)
 
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=dev)
+    FL = bl.FLAG_PDL
 
     def step(ev=None):
+        """One pass: for M in (1, 8), for every layer and projection: RMSNorm + int8
+        quantization (writing the tensor-core operand form) and the contraction."""
         i = 0
+        flags = 0 if ev is not None else FL
         for M in wl.tokens:
             for row in weights:
                 for (p, packed, w_scale) in row:
-                    bl.bitlinear_quant_act(xs[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)], act_scale=sc[(M, p.K)])
+                    bl.bitlinear_quant_act(xs[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)],
+                                           act_scale=sc[(M, p.K)], x_ops=ops[(M, p.K)], flags=flags,
+                                           stream=stream)
                     if ev is not None:
                         ev[i][0].record(stream)
-                    bl.bitlinear_forward(xq[(M, p.K)], sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
-                                         y=ys[(M, p.N)], workspace=fwd_ws[(M, p.N, p.K)])
+                    bl.bitlinear_forward(None, sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
+                                         y=ys[(M, p.N)], x_ops=ops[(M, p.K)], flags=flags, K=p.K,
+                                         stream=stream)
                     if ev is not None:
                         ev[i][1].record(stream)
                     i += 1
@@ -322,40 +325,58 @@ def our_arm(args):
         if pg is not None:
             pg.barrier()
 
-    # ---- warmup: W steps, then more untimed steps until ~1 s has passed (clock ramp-up)
+    # ---- the step as one CUDA graph (kernels chained by programmatic dependent launch)
+    with torch.cuda.stream(stream):
+        step()                                   # eager warm-up (module load, first launches)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        l0 = bl.bitlinear_kernel_launches()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        launches_per_step = bl.bitlinear_kernel_launches() - l0
+    torch.cuda.synchronize()
+
+    # ---- warmup: W replays, then more until ~1 s has passed (clock ramp-up)
     t0 = time.perf_counter()
     n = 0
     while n < args.warmup or time.perf_counter() - t0 < 1.0:
-        step()
+        graph.replay()
         n += 1
         if n % 20 == 0:
             torch.cuda.synchronize()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, per-launch events on the forward kernels
-    per_step_launches = len(alg_bytes_fwd)
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(per_step_launches)] for _ in range(args.steps)]
+    # ---- timed region: K replays of the step
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = bl.bitlinear_kernel_launches()
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
-        start.record(stream)
-        for s in range(args.steps):
-            step(evs[s])
-        end.record(stream)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for s in range(args.steps):
+                graph.replay()
+            end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    launches = bl.bitlinear_kernel_launches() - launches0
+    launches = launches_per_step * args.steps
     ms = start.elapsed_time(end) / args.steps
-    fwd_ms = [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps
-              for i in range(per_step_launches)]
     if pg is not None:
         t = torch.tensor([ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
     value = world * packed_bytes_step / (ms * 1e-3) / 1e9
+
+    # ---- per-launch durations of the contraction kernel: the same K steps eagerly, with
+    #      CUDA events on the launching stream around every forward (no overlap between kernels)
+    per_step_launches = len(alg_bytes_fwd)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(per_step_launches)] for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for s in range(args.steps):
+            step(evs[s])
+    torch.cuda.synchronize()
+    fwd_ms = [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps
+              for i in range(per_step_launches)]
 
     # ---- end to end through the public API: pinned host inputs in, bf16 outputs out
     host_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
@@ -373,22 +394,23 @@ def our_arm(args):
             for row in weights:
                 for (p, packed, w_scale) in row:
                     dev_x[(M, p.K)].copy_(host_x[(M, p.K)], non_blocking=True)
-                    q, s_ = bl.bitlinear_quant_act(dev_x[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)],
-                                                   act_scale=sc[(M, p.K)])
-                    y = bl.bitlinear_forward(q, s_, packed, w_scale, out_dtype=torch.bfloat16, y=ys[(M, p.N)],
-                                             workspace=fwd_ws[(M, p.N, p.K)])
+                    bl.bitlinear_quant_act(dev_x[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)],
+                                           act_scale=sc[(M, p.K)], x_ops=ops[(M, p.K)], flags=FL)
+                    y = bl.bitlinear_forward(None, sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
+                                             y=ys[(M, p.N)], x_ops=ops[(M, p.K)], flags=FL, K=p.K)
                     host_y[(M, p.N)].copy_(y, non_blocking=True)
 
-    for _ in range(max(args.warmup, 1)):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
     if pg is not None:
         t = torch.tensor([e2e_ms], device=dev)
@@ -399,10 +421,11 @@ def our_arm(args):
     # ---- roofline of the dominant kernel (the contraction)
     hbm, bf16_tf, peak_src = measured_peaks()
     achieved = sum(alg_bytes_fwd) / (sum(fwd_ms) * 1e-3) / 1e9
-    traffic = traffic_record(os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc", "gemv.cu"))
+    traffic = traffic_record(os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc", "decode_mma.cu"))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic, "peak_source": peak_src,
-                "kernel": "bitlinear_forward (ternary contraction + dequant)",
+                "kernel": "decode_mma_kernel (bitlinear_forward: ternary contraction + dequant)",
+                "timing": "per-launch CUDA events on the launching stream, K eager steps after the timed graph replays",
                 "alg_bytes_per_launch": sum(alg_bytes_fwd) / len(alg_bytes_fwd),
                 "avg_launch_us": sum(fwd_ms) / len(fwd_ms) * 1e3,
                 "share_of_step": sum(fwd_ms) / ms if ms > 0 else None}
@@ -423,6 +446,7 @@ def our_arm(args):
                    "projections": [[p.name, p.K, p.N] for p in wl.projections],
                    "packed_bytes_per_step": packed_bytes_step,
                    "l2": "no flush: 520 MB of distinct packed weights per pass (> 4x the 126 MB L2)",
+                   "launch": "one CUDA graph per step; kernels chained by programmatic dependent launch",
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),

@@ -25,13 +25,14 @@ __all__ = [
     "BitLinearError", "lib", "library_path", "bitlinear_pack_weights", "bitlinear_quant_act",
     "bitlinear_forward", "bitlinear_get_device_error", "bitlinear_packed_bytes",
     "bitlinear_forward_workspace_bytes", "bitlinear_pack_workspace_bytes", "OUT_F32", "OUT_BF16",
-    "STATUS", "bitlinear_kernel_launches",
+    "STATUS", "bitlinear_kernel_launches", "bitlinear_act_ops_bytes", "FLAG_PDL",
 ]
 
 OUT_F32 = 0
 OUT_BF16 = 1
+FLAG_PDL = 1
 STATUS = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_DTYPE", 5: "ERR_DEVICE",
-          6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_WORKSPACE", 9: "ERR_NONFINITE"}
+          6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_WORKSPACE", 9: "ERR_NONFINITE", 10: "ERR_FLAGS"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libbitlinear.so")
@@ -55,6 +56,7 @@ def lib() -> ctypes.CDLL:
                 "`python -m bitlinear_rmsnorm_token_int8_b300.build` (no CPU fallback exists)")
         L = ctypes.CDLL(library_path)
         P, I64, SZ, F, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_int
+        U = ctypes.c_uint
         L.bitlinear_status_string.argtypes = [I]
         L.bitlinear_status_string.restype = ctypes.c_char_p
         L.bitlinear_abi_version.restype = I
@@ -65,11 +67,13 @@ def lib() -> ctypes.CDLL:
         L.bitlinear_pack_workspace_bytes.restype = SZ
         L.bitlinear_pack_weights.argtypes = [P, I64, I64, F, P, P, P, P, SZ, P]
         L.bitlinear_pack_weights.restype = I
-        L.bitlinear_quant_act.argtypes = [P, P, F, I64, I64, P, P, P]
+        L.bitlinear_act_ops_bytes.argtypes = [I64, I64]
+        L.bitlinear_act_ops_bytes.restype = SZ
+        L.bitlinear_quant_act.argtypes = [P, P, F, I64, I64, P, P, P, U, P]
         L.bitlinear_quant_act.restype = I
         L.bitlinear_forward_workspace_bytes.argtypes = [I64, I64, I64]
         L.bitlinear_forward_workspace_bytes.restype = SZ
-        L.bitlinear_forward.argtypes = [P, P, P, P, I64, I64, I64, I, P, P, P, SZ, P]
+        L.bitlinear_forward.argtypes = [P, P, P, P, P, I64, I64, I64, I, P, P, P, SZ, U, P]
         L.bitlinear_forward.restype = I
         L.bitlinear_get_device_error.argtypes = [P]
         L.bitlinear_get_device_error.restype = I
@@ -118,14 +122,22 @@ def bitlinear_forward_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(lib().bitlinear_forward_workspace_bytes(M, N, K))
 
 
+def bitlinear_act_ops_bytes(M: int, K: int) -> int:
+    return int(lib().bitlinear_act_ops_bytes(M, K))
+
+
 def bitlinear_pack_weights(W: torch.Tensor, eps: float = 1e-5, packed=None, w_scale=None,
                            gamma=None, workspace=None, stream=None):
-    """Ternarize + pack latent weights W [N,K] fp32 (CUDA).  Returns (packed, w_scale, gamma)."""
+    """Ternarize + pack latent weights W [N,K] fp32 (CUDA).  Returns (packed, w_scale, gamma).
+
+    ``packed`` is a flat uint8 tensor of :func:`bitlinear_packed_bytes` bytes in the
+    tile-major layout (see :mod:`.layout` for the index map to the canonical [N, K/4]).
+    """
     _cuda(W, "W", torch.float32)
     N, K = W.shape
     dev = W.device
     if packed is None:
-        packed = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+        packed = torch.empty(max(bitlinear_packed_bytes(N, K), 16), dtype=torch.uint8, device=dev)
     if w_scale is None:
         w_scale = torch.empty(N, dtype=torch.float32, device=dev)
     if gamma is None:
@@ -139,10 +151,13 @@ def bitlinear_pack_weights(W: torch.Tensor, eps: float = 1e-5, packed=None, w_sc
 
 
 def bitlinear_quant_act(x: torch.Tensor, gain=None, rms_eps: float = 1e-5, x_q=None,
-                        act_scale=None, stream=None):
-    """RMSNorm + per-token int8 quantization of x [M,K] bf16 (CUDA).  Returns (x_q, act_scale).
+                        act_scale=None, x_ops=None, flags: int = 0, stream=None):
+    """RMSNorm + per-token int8 quantization of x [M,K] bf16 (CUDA).
 
     ``rms_eps < 0`` skips RMSNorm; ``gain`` is the RMSNorm weight (bf16 [K]) or None.
+    ``x_ops``: None (not produced), True (allocate) or a uint8 tensor of
+    :func:`bitlinear_act_ops_bytes` bytes that receives the operand form of the codes.
+    Returns (x_q, act_scale) or, when x_ops is requested, (x_q, act_scale, x_ops).
     """
     _cuda(x, "x", torch.bfloat16)
     M, K = x.shape
@@ -152,31 +167,48 @@ def bitlinear_quant_act(x: torch.Tensor, gain=None, rms_eps: float = 1e-5, x_q=N
         x_q = torch.empty((M, K), dtype=torch.int8, device=x.device)
     if act_scale is None:
         act_scale = torch.empty(max(M, 1) + 3, dtype=torch.float32, device=x.device)[:M]
+    want_ops = x_ops is not None
+    if x_ops is True:
+        x_ops = torch.empty(max(bitlinear_act_ops_bytes(M, K), 16), dtype=torch.uint8, device=x.device)
     _check("bitlinear_quant_act", lib().bitlinear_quant_act(
-        _ptr(x), _ptr(gain), float(rms_eps), M, K, _ptr(x_q), _ptr(act_scale), _stream(stream)))
-    return x_q, act_scale
+        _ptr(x), _ptr(gain), float(rms_eps), M, K, _ptr(x_q), _ptr(act_scale),
+        _ptr(x_ops) if want_ops else None, int(flags), _stream(stream)))
+    return (x_q, act_scale, x_ops) if want_ops else (x_q, act_scale)
 
 
-def bitlinear_forward(x_q: torch.Tensor, act_scale: torch.Tensor, packed: torch.Tensor,
+def bitlinear_forward(x_q, act_scale: torch.Tensor, packed: torch.Tensor,
                       w_scale: torch.Tensor, out_dtype=torch.bfloat16, y=None, acc_debug=None,
-                      workspace=None, stream=None):
-    """y [M,N] = dequant(x_q . W_q^T) (CUDA).  ``acc_debug``: optional int32 [M,N] out."""
-    _cuda(x_q, "x_q", torch.int8)
+                      workspace=None, x_ops=None, flags: int = 0, K: int | None = None, stream=None):
+    """y [M,N] = dequant(x_q . W_q^T) (CUDA).  ``acc_debug``: optional int32 [M,N] out.
+
+    N is ``w_scale``'s length.  ``x_ops`` (from :func:`bitlinear_quant_act`) skips the
+    conversion of x_q; x_q may then be None, and ``K`` must be given.
+    """
     _cuda(packed, "packed", torch.uint8)
-    M, K = x_q.shape
-    N = packed.shape[0]
+    _cuda(act_scale, "act_scale", torch.float32)
+    _cuda(w_scale, "w_scale", torch.float32)
+    if x_q is not None:
+        _cuda(x_q, "x_q", torch.int8)
+        M, K = x_q.shape
+    else:
+        if x_ops is None or K is None:
+            raise ValueError("x_q, or x_ops and K, are required")
+        M = act_scale.shape[0]
+    N = w_scale.shape[0]
+    if packed.numel() < bitlinear_packed_bytes(N, K):
+        raise ValueError("packed is smaller than bitlinear_packed_bytes(N, K)")
     code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(out_dtype)
     if code is None:
         raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     if y is None:
-        y = torch.empty((M, N), dtype=out_dtype, device=x_q.device)
-    need = bitlinear_forward_workspace_bytes(M, N, K)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x_q.device)
+        y = torch.empty((M, N), dtype=out_dtype, device=packed.device)
+    if x_ops is None and workspace is None:
+        need = bitlinear_forward_workspace_bytes(M, N, K)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=packed.device)
     _check("bitlinear_forward", lib().bitlinear_forward(
-        _ptr(x_q), _ptr(act_scale), _ptr(packed), _ptr(w_scale), M, N, K, code, _ptr(y),
+        _ptr(x_q), _ptr(act_scale), _ptr(x_ops), _ptr(packed), _ptr(w_scale), M, N, K, code, _ptr(y),
         _ptr(acc_debug), _ptr(workspace), 0 if workspace is None else workspace.numel(),
-        _stream(stream)))
+        int(flags), _stream(stream)))
     return y
 
 

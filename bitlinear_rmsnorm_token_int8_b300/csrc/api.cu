@@ -58,6 +58,8 @@ const DeviceState* current_device() {
   return s.ok ? &s : nullptr;
 }
 
+constexpr unsigned kKnownFlags = BITLINEAR_FLAG_PDL;
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bitlinear_status from_cuda(cudaError_t e) {
@@ -98,6 +100,7 @@ const char* bitlinear_status_string(bitlinear_status status) {
     case BITLINEAR_ERR_TIMEOUT: return "bounded wait timed out on the device";
     case BITLINEAR_ERR_WORKSPACE: return "workspace missing or too small";
     case BITLINEAR_ERR_NONFINITE: return "non-finite latent weight";
+    case BITLINEAR_ERR_FLAGS: return "unknown flag bits";
   }
   return "unknown status";
 }
@@ -107,8 +110,8 @@ int bitlinear_abi_version(void) { return 1; }
 uint64_t bitlinear_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 size_t bitlinear_packed_bytes(int64_t N, int64_t K) {
-  if (N < 0 || K < 0) return 0;
-  return (size_t)(N * (K / 4));
+  if (N < 1 || K < 4 || K % 4 != 0 || N > (int64_t(1) << 32) || K > (int64_t(1) << 32)) return 0;
+  return (size_t)packed_layout_bytes(N, K);
 }
 
 size_t bitlinear_pack_workspace_bytes(int64_t, int64_t) { return kPackWorkspaceBytes; }
@@ -129,21 +132,29 @@ bitlinear_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, fl
                                        dev->err_word, static_cast<cudaStream_t>(stream)));
 }
 
+size_t bitlinear_act_ops_bytes(int64_t M, int64_t K) {
+  if (M < 0 || K < 1) return 0;
+  return act_ops_bytes(M, K);
+}
+
 bitlinear_status bitlinear_quant_act(const void* x_bf16, const void* gain_bf16, float rms_eps,
                                      int64_t M, int64_t K, int8_t* x_q, float* act_scale,
-                                     void* stream) {
+                                     void* x_ops, unsigned flags, void* stream) {
   if (M < 0 || M > (int64_t(1) << 31) - 1 || K < 8 || K > 65536 || K % 8 != 0)
     return BITLINEAR_ERR_SHAPE;
+  if (flags & ~kKnownFlags) return BITLINEAR_ERR_FLAGS;
   if (M == 0) return BITLINEAR_OK;
   if (!x_bf16 || !x_q || !act_scale) return BITLINEAR_ERR_NULL;
   if (!aligned16(x_bf16) || !aligned16(x_q) || !aligned16(act_scale) ||
-      (gain_bf16 && !aligned16(gain_bf16)))
+      (gain_bf16 && !aligned16(gain_bf16)) || (x_ops && !aligned16(x_ops)))
     return BITLINEAR_ERR_ALIGN;
   const DeviceState* dev = current_device();
   if (!dev) return BITLINEAR_ERR_DEVICE;
   return from_cuda(launch_quant_act(static_cast<const uint16_t*>(x_bf16),
                                     static_cast<const uint16_t*>(gain_bf16), rms_eps, M, K, x_q,
-                                    act_scale, static_cast<cudaStream_t>(stream)));
+                                    act_scale, static_cast<uint8_t*>(x_ops),
+                                    (flags & BITLINEAR_FLAG_PDL) != 0,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -151,29 +162,33 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return forward_workspace_bytes(M, N, K);
 }
 
-bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale,
+bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, const void* x_ops,
                                    const uint8_t* packed, const float* w_scale, int64_t M,
                                    int64_t N, int64_t K, int out_dtype, void* y,
                                    int32_t* acc_debug, void* workspace, size_t workspace_bytes,
-                                   void* stream) {
+                                   unsigned flags, void* stream) {
   if (M < 0 || M > (int64_t(1) << 24) || N < 16 || N % 16 != 0 || N > (int64_t(1) << 24) ||
       K < 128 || K % 128 != 0 || K > 65536)
     return BITLINEAR_ERR_SHAPE;
   if (out_dtype != BITLINEAR_OUT_F32 && out_dtype != BITLINEAR_OUT_BF16) return BITLINEAR_ERR_DTYPE;
+  if (flags & ~kKnownFlags) return BITLINEAR_ERR_FLAGS;
   if (M == 0) return BITLINEAR_OK;
-  if (!x_q || !act_scale || !packed || !w_scale || !y) return BITLINEAR_ERR_NULL;
-  if (!aligned16(x_q) || !aligned16(act_scale) || !aligned16(packed) || !aligned16(w_scale) ||
-      !aligned16(y) || (acc_debug && !aligned16(acc_debug)))
+  if (!act_scale || !packed || !w_scale || !y || (!x_q && !x_ops)) return BITLINEAR_ERR_NULL;
+  if ((x_q && !aligned16(x_q)) || (x_ops && !aligned16(x_ops)) || !aligned16(act_scale) ||
+      !aligned16(packed) || !aligned16(w_scale) || !aligned16(y) ||
+      (acc_debug && !aligned16(acc_debug)))
     return BITLINEAR_ERR_ALIGN;
-  const size_t need = forward_workspace_bytes(M, N, K);
-  if (need > 0) {
+  if (!x_ops) {
+    const size_t need = forward_workspace_bytes(M, N, K);
     if (!workspace || workspace_bytes < need) return BITLINEAR_ERR_WORKSPACE;
     if (!aligned16(workspace)) return BITLINEAR_ERR_ALIGN;
   }
   const DeviceState* dev = current_device();
   if (!dev) return BITLINEAR_ERR_DEVICE;
-  return from_cuda(launch_forward(x_q, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
-                                  workspace, dev->err_word, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_forward(x_q, act_scale, static_cast<const uint8_t*>(x_ops), packed,
+                                  w_scale, M, N, K, out_dtype, y, acc_debug, workspace,
+                                  dev->err_word, (flags & BITLINEAR_FLAG_PDL) != 0,
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 bitlinear_status bitlinear_get_device_error(void* stream) {

@@ -6,26 +6,21 @@
 
 namespace bitlinear {
 
-cudaError_t launch_gemv_dp4a(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
-                             const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
-                             void* y, int32_t* acc_debug, cudaStream_t stream);
+size_t forward_workspace_bytes(int64_t M, int64_t, int64_t K) { return act_ops_bytes(M, K); }
 
-size_t forward_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
-
-cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
-                           const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
-                           void* y, int32_t* acc_debug, void*, int*, cudaStream_t stream) {
-  // token tiles of at most 65535 * 8 rows per launch (grid.y limit)
-  const int64_t max_tokens = 65535LL * 8;
-  for (int64_t t0 = 0; t0 < M; t0 += max_tokens) {
-    const int64_t m = (M - t0 < max_tokens) ? (M - t0) : max_tokens;
-    const size_t esz = out_dtype == 0 ? 4 : 2;
-    cudaError_t e = launch_gemv_dp4a(x_q + t0 * K, act_scale + t0, packed, w_scale, m, N, K, out_dtype,
-                                     static_cast<char*>(y) + (size_t)t0 * N * esz,
-                                     acc_debug ? acc_debug + t0 * N : nullptr, stream);
+cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint8_t* x_ops,
+                           const uint8_t* packed, const float* w_scale, int64_t M, int64_t N,
+                           int64_t K, int out_dtype, void* y, int32_t* acc_debug, void* workspace,
+                           int* dev_err, bool pdl, cudaStream_t stream) {
+  if (!x_ops) {
+    uint8_t* ops = static_cast<uint8_t*>(workspace);
+    cudaError_t e = launch_act_ops_from_codes(x_q, M, K, ops, pdl, stream);
     if (e != cudaSuccess) return e;
+    x_ops = ops;
+    pdl = true;   // the operand kernel just enqueued is ours: overlap with it is safe
   }
-  return cudaSuccess;
+  return launch_decode_mma(x_ops, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
+                           dev_err, pdl, stream);
 }
 
 }  // namespace bitlinear

@@ -13,6 +13,18 @@ namespace bitlinear {
 constexpr int kDevErrTimeout = 7;
 constexpr int kDevErrNonFinite = 9;
 
+// ---- packed weight layout -------------------------------------------------
+// Tile-major and pre-swizzled for the contraction kernels: rows in tiles of 16
+// (N padded to a multiple of 16), K in segments of 512 (padded with zero codes),
+// and per (tile, segment) a contiguous 2048-byte block of 16 rows x 128 bytes in
+// which the 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
+// Byte b of row n's canonical packed row (b = k / 4) lives at
+//   ((n / 16) * nseg + b / 128) * 2048 + (n % 16) * 128 + (((b % 128) / 16) ^ (n % 8)) * 16 + b % 16.
+constexpr int64_t kSegK = 512;
+inline int64_t packed_nseg(int64_t K) { return (K + kSegK - 1) / kSegK; }
+inline int64_t packed_tiles(int64_t N) { return (N + 15) / 16; }
+inline int64_t packed_layout_bytes(int64_t N, int64_t K) { return packed_tiles(N) * packed_nseg(K) * 2048; }
+
 // ---- pack_weights --------------------------------------------------------
 // Workspace layout (bytes): [0, 2048) 256 uint64 exponent bins of sum|W|,
 // [2048, 2056) gamma and d = fl32(gamma + eps) as two floats.
@@ -24,18 +36,33 @@ cudaError_t launch_pack_weights(const float* W, int64_t N, int64_t K, float eps,
                                 cudaStream_t stream);
 
 // ---- quant_act -----------------------------------------------------------
+// x_ops: optional tensor-core operand planes of the codes (act_ops.cuh), or nullptr.
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,
-                             int64_t K, int8_t* x_q, float* act_scale, cudaStream_t stream);
+                             int64_t K, int8_t* x_q, float* act_scale, uint8_t* x_ops, bool pdl,
+                             cudaStream_t stream);
+
+// ---- activation operands ---------------------------------------------------
+size_t act_ops_bytes(int64_t M, int64_t K);
+cudaError_t launch_act_ops_from_codes(const int8_t* x_q, int64_t M, int64_t K, uint8_t* ops,
+                                      bool pdl, cudaStream_t stream);
 
 // ---- forward ---------------------------------------------------------------
 size_t forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
-cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
-                           const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
-                           void* y, int32_t* acc_debug, void* workspace, int* dev_err,
-                           cudaStream_t stream);
+// x_ops may be nullptr: the operands are then derived from x_q into the workspace.
+cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint8_t* x_ops,
+                           const uint8_t* packed, const float* w_scale, int64_t M, int64_t N,
+                           int64_t K, int out_dtype, void* y, int32_t* acc_debug, void* workspace,
+                           int* dev_err, bool pdl, cudaStream_t stream);
+
+cudaError_t launch_decode_mma(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
+                              const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
+                              void* y, int32_t* acc_debug, int* dev_err, bool pdl,
+                              cudaStream_t stream);
 
 int num_sms();
+
+
 
 // Checks that the calling thread's current device is usable (sm_103) and returns
 // the device address of its error word, or nullptr.

@@ -15,7 +15,8 @@
 //      integer (units of 2^-149), divides by N*K with a long division, and
 //      rounds the quotient to binary32 (nearest, ties to even) from the
 //      quotient bits, a round bit and a sticky bit.
-//   3. ternarize_pack: W_q = sign(W) where 2|W| > d = fl32(gamma + eps), else 0.
+//   3. ternarize_pack: W_q = sign(W) where 2|W| > d = fl32(gamma + eps), else 0,
+//      written in the tile-major layout of the contraction kernels (internal.h).
 //      This is exactly Round(W/d) clipped to [-1, 1]: |W/d| = 1/2 is a tie that
 //      rounds to the even value 0, and every |W/d| > 1/2 rounds to a non-zero
 //      integer that the clip maps to sign(W).  2|W| is exact in binary32.
@@ -115,25 +116,43 @@ __global__ void gamma_finalize_kernel(const unsigned long long* __restrict__ bin
   if (gamma_out) *gamma_out = gamma;
 }
 
-// One thread per packed byte (four weights).
-__global__ void ternarize_pack_kernel(const float4* __restrict__ w4, int64_t nbytes, int64_t kb,
-                                      const float* __restrict__ gd, uint8_t* __restrict__ packed,
-                                      float* __restrict__ w_scale) {
+// One thread per 16-byte chunk of the tiled layout (64 weights of one row; see
+// internal.h): codes of rows >= N or k >= K are 0.
+__global__ void ternarize_pack_kernel(const float* __restrict__ W, int64_t N, int64_t K,
+                                      int64_t nseg, int64_t chunks, const float* __restrict__ gd,
+                                      uint8_t* __restrict__ packed, float* __restrict__ w_scale) {
   const float gamma = gd[0];
   const float d = gd[1];
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 v = __ldg(w4 + i);
-    const float f[4] = {v.x, v.y, v.z, v.w};
-    uint32_t byte = 0;
+  for (int64_t ci = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; ci < chunks;
+       ci += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t blk = ci >> 7;
+    const int within = (int)(ci & 127);
+    const int r = within >> 3, c = (within & 7) ^ (r & 7);     // logical chunk of this position
+    const int64_t tile = blk / nseg, seg = blk - tile * nseg;
+    const int64_t n = tile * 16 + r;
+    const int64_t k0 = seg * 512 + c * 64;
+    uint32_t out[4] = {0u, 0u, 0u, 0u};
+    if (n < N) {
+      const float* wr = W + n * K;
+#pragma unroll 4
+      for (int q = 0; q < 16; ++q) {             // 16 groups of four weights = 16 bytes
+        const int64_t k = k0 + 4 * q;
+        if (k < K) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(wr + k));
+          const float f[4] = {v.x, v.y, v.z, v.w};
+          uint32_t byte = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float a = __fmul_rn(2.0f, fabsf(f[j]));
-      const uint32_t code = (a > d) ? (f[j] > 0.0f ? 1u : 2u) : 0u;
-      byte |= code << (2 * j);
+          for (int j = 0; j < 4; ++j) {
+            const float a = __fmul_rn(2.0f, fabsf(f[j]));
+            const uint32_t code = (a > d) ? (f[j] > 0.0f ? 1u : 2u) : 0u;
+            byte |= code << (2 * j);
+          }
+          out[q >> 2] |= byte << (8 * (q & 3));
+        }
+      }
+      if (seg == 0 && c == 0) w_scale[n] = gamma;
     }
-    packed[i] = (uint8_t)byte;
-    if (i % kb == 0) w_scale[i / kb] = gamma;
+    *reinterpret_cast<uint4*>(packed + (ci << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
@@ -155,9 +174,11 @@ cudaError_t launch_pack_weights(const float* W, int64_t N, int64_t K, float eps,
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   gamma_finalize_kernel<<<1, 32, 0, stream>>>(bins, (uint64_t)(N * K), eps, gd, gamma_out);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  int64_t pblocks = (n4 + 255) / 256;
+  const int64_t nseg = packed_nseg(K);
+  const int64_t chunks = packed_layout_bytes(N, K) / 16;
+  int64_t pblocks = (chunks + 255) / 256;
   if (pblocks > (int64_t)sms * 16) pblocks = (int64_t)sms * 16;
-  ternarize_pack_kernel<<<(unsigned)pblocks, 256, 0, stream>>>(w4, n4, K / 4, gd, packed, w_scale);
+  ternarize_pack_kernel<<<(unsigned)pblocks, 256, 0, stream>>>(W, N, K, nseg, chunks, gd, packed, w_scale);
   count_launches(3);
   return cudaGetLastError();
 }

@@ -7,17 +7,29 @@
 //
 // One CTA per token row.  The row is read once from HBM with 16-byte loads and
 // kept in registers; a block reduction gives max|x*g| (exact: max is order
-// free) and sum x^2 (fp32 pairwise inside a thread, fp64 across threads).
+// free) and sum x^2.  No fp64 is used (it is slow on this GPU): x^2 is exact in
+// fp32 (bf16 squared), and the sum is carried as an unevaluated pair hi + lo
+// of fp32 numbers with error-free additions (Knuth's TwoSum), i.e. to about
+// 2^-44 relative, before it is rounded once to fp32.
+//
+// sigma = max|x*g| * r / 127 with r = 1/sqrt(sum/K + eps): every step is one
+// IEEE round-to-nearest operation, so with u = 2^-24 the result is within
+// 4.5 u (2.7e-7) of the exact value: sum u, /K 2u, +eps 3u, rsqrt 2.5u,
+// *m 3.5u, /127 4.5u.
 //
 // Codes.  r > 0 is one number per row, so Round(127 n/max|n|) with n = x*r*g
 // equals Round(127 p/max|p|) with p = x*g, and p is exact in fp32 (two 8-bit
 // significands).  The kernel forms t = p * fl(127/m) (relative error <= 2^-23,
 // i.e. |t - 127p/m| < 1.6e-5) and takes rint(t) unless t lies within 2^-15 of
-// a half-integer; there it decides exactly in fp64, where 127*p and
-// (floor(t)+0.5)*m are both exact products, with ties going to the even code.
+// a half-integer.  There it decides on the sign of 127 p - (floor(t) + 1/2) m:
+// 127 p is exact (at most 16 + 7 significant bits), and one fused multiply-add
+// forms the difference with a single rounding, which cannot change its sign;
+// an exact zero is a tie and goes to the even code.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "act_ops.cuh"
+#include "device_util.cuh"
 #include "internal.h"
 
 namespace bitlinear {
@@ -42,140 +54,194 @@ __device__ __forceinline__ int quant_code(float p, float s, float m) {
   if (dist > 3.0517578125e-05f) {          // 2^-15
     q = rintf(t);
   } else {
-    const double a = 127.0 * (double)p;     // exact
-    const double h = ((double)f + 0.5) * (double)m;  // exact: 9-bit * 24-bit
-    if (a > h) q = f + 1.0f;
-    else if (a < h) q = f;
+    const float a = __fmul_rn(127.0f, p);                       // exact
+    const float d = __fmaf_rn(-__fadd_rn(f, 0.5f), m, a);       // sign of 127p - (f+1/2)m
+    if (d > 0.0f) q = f + 1.0f;
+    else if (d < 0.0f) q = f;
     else q = (fmodf(f, 2.0f) == 0.0f) ? f : f + 1.0f;
   }
   q = fminf(fmaxf(q, -128.0f), 127.0f);
   return (int)q;
 }
 
+// Error-free sum of two fp32 numbers: s + e == a + b exactly (Knuth).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// (h1 + l1) + (h2 + l2) as a renormalised pair.
+__device__ __forceinline__ void pair_add(float& h1, float& l1, float h2, float l2) {
+  float s, e;
+  two_sum(h1, h2, s, e);
+  e = __fadd_rn(e, __fadd_rn(l1, l2));
+  h1 = __fadd_rn(s, e);
+  l1 = __fsub_rn(e, __fsub_rn(h1, s));
+}
+
 // eight bf16 ones
 __device__ __constant__ uint4 kOnes = {0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u};
 
-template <int VPT>
+// A thread owns units of 16 consecutive inputs (two 16-byte bf16 vectors), so
+// that it can store the operand form of a unit with two 16-byte stores.
+template <int UPT>
 __global__ void __launch_bounds__(1024)
 quant_act_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gain, float rms_eps,
-                 int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale) {
+                 int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale,
+                 uint8_t* __restrict__ x_ops, int64_t M) {
+  pdl_wait();                                // x may be the previous kernel's output
+  pdl_launch_dependents();
   const int V = K >> 3;                      // 16-byte vectors per row
+  const int U = (V + 1) >> 1;                // units of 16 inputs
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int T = blockDim.x;
   const uint4* xr = x + (size_t)row * V;
 
-  uint4 xv[VPT];
+  uint4 xv[UPT][2];
   float amax = 0.0f;
-  float part[VPT];
+  float hi = 0.0f, lo = 0.0f;                // sum of x^2 as hi + lo
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int v = tid + i * T;
-    part[i] = 0.0f;
-    if (v < V) {
-      xv[i] = __ldg(xr + v);
-      float xf[8], gf[8];
-      unpack8(xv[i], xf);
-      unpack8(gain ? __ldg(gain + v) : kOnes, gf);
-      float sq[8];
+  for (int i = 0; i < UPT; ++i) {
+    const int u = tid + i * T;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        amax = fmaxf(amax, fabsf(__fmul_rn(xf[j], gf[j])));
-        sq[j] = __fmul_rn(xf[j], xf[j]);
+    for (int hv = 0; hv < 2; ++hv) {
+      const int v = 2 * u + hv;
+      if (u < U && v < V) {
+        xv[i][hv] = __ldg(xr + v);
+        float xf[8], gf[8];
+        unpack8(xv[i][hv], xf);
+        unpack8(gain ? __ldg(gain + v) : kOnes, gf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          amax = fmaxf(amax, fabsf(__fmul_rn(xf[j], gf[j])));
+          float s_, e_;
+          two_sum(hi, __fmul_rn(xf[j], xf[j]), s_, e_);   // x^2 is exact in fp32
+          hi = s_;
+          lo = __fadd_rn(lo, e_);
+        }
+      } else {
+        xv[i][hv] = make_uint4(0u, 0u, 0u, 0u);
       }
-      part[i] = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
-                          __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
     }
   }
-  // pairwise sum of the thread's vectors
-#pragma unroll
-  for (int w = 1; w < VPT; w <<= 1)
-#pragma unroll
-    for (int i = 0; i + w < VPT; i += 2 * w) part[i] = __fadd_rn(part[i], part[i + w]);
-  double ss = (double)part[0];
 
-  // block reduction: max (exact) and sum of squares (fp64)
+  // block reduction: max (exact) and the pair sum of squares
   __shared__ float s_max[32];
-  __shared__ double s_ss[32];
+  __shared__ float2 s_ss[32];
   __shared__ float s_m;
-  __shared__ double s_sum;
+  __shared__ float s_sum;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    pair_add(hi, lo, h2, l2);
   }
   const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;
-  if (lane == 0) { s_max[warp] = amax; s_ss[warp] = ss; }
+  if (lane == 0) { s_max[warp] = amax; s_ss[warp] = make_float2(hi, lo); }
   __syncthreads();
   if (warp == 0) {
     float a = lane < nwarps ? s_max[lane] : 0.0f;
-    double s = lane < nwarps ? s_ss[lane] : 0.0;
+    float2 p2 = lane < nwarps ? s_ss[lane] : make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-      s += __shfl_xor_sync(0xffffffffu, s, o);
+      const float h2 = __shfl_xor_sync(0xffffffffu, p2.x, o), l2 = __shfl_xor_sync(0xffffffffu, p2.y, o);
+      pair_add(p2.x, p2.y, h2, l2);
     }
-    if (lane == 0) { s_m = a; s_sum = s; }
+    if (lane == 0) { s_m = a; s_sum = __fadd_rn(p2.x, p2.y); }
   }
   __syncthreads();
 
   const float m = fmaxf(s_m, 1e-8f);
   const float s = __fdiv_rn(127.0f, m);
   if (tid == 0) {
-    double sigma = (double)m / 127.0;
-    if (rms_eps >= 0.0f) sigma = sigma / sqrt(s_sum / (double)K + (double)rms_eps);
-    act_scale[row] = (float)sigma;
+    float sigma = __fdiv_rn(m, 127.0f);
+    if (rms_eps >= 0.0f) {
+      const float ms = __fdiv_rn(s_sum, (float)K);
+      const float r = __frsqrt_rn(__fadd_rn(ms, rms_eps));
+      sigma = __fdiv_rn(__fmul_rn(m, r), 127.0f);
+    }
+    act_scale[row] = sigma;
   }
 
   uint2* qr = reinterpret_cast<uint2*>(x_q + (size_t)row * K);
+  const int64_t Kp = act_ops_kpad(K);
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int v = tid + i * T;
-    if (v < V) {
-      float xf[8], gf[8];
-      unpack8(xv[i], xf);
-      unpack8(gain ? __ldg(gain + v) : kOnes, gf);
-      uint32_t lo = 0, hi = 0;
+  for (int i = 0; i < UPT; ++i) {
+    const int u = tid + i * T;
+    if (u < U) {
+      int q[16];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        lo |= (uint32_t)(quant_code(__fmul_rn(xf[j], gf[j]), s, m) & 0xff) << (8 * j);
-        hi |= (uint32_t)(quant_code(__fmul_rn(xf[j + 4], gf[j + 4]), s, m) & 0xff) << (8 * j);
+      for (int hv = 0; hv < 2; ++hv) {
+        float xf[8], gf[8];
+        unpack8(xv[i][hv], xf);
+        const int v = 2 * u + hv;
+        unpack8((gain && v < V) ? __ldg(gain + v) : kOnes, gf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q[8 * hv + j] = quant_code(__fmul_rn(xf[j], gf[j]), s, m);
+        if (v < V) {
+          uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            w0 |= (uint32_t)(q[8 * hv + j] & 0xff) << (8 * j);
+            w1 |= (uint32_t)(q[8 * hv + j + 4] & 0xff) << (8 * j);
+          }
+          qr[v] = make_uint2(w0, w1);
+        }
       }
-      qr[v] = make_uint2(lo, hi);
+      if (x_ops) write_act_ops16(x_ops, M, row, (int64_t)u << 4, Kp, q);   // zero x -> zero code
     }
+  }
+  if (x_ops) {                               // zero operands of the padding up to Kp
+    int z[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) z[j] = 0;
+    for (int u = U + tid; u < (int)(Kp >> 4); u += T) write_act_ops16(x_ops, M, row, (int64_t)u << 4, Kp, z);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,
-                             int64_t K, int8_t* x_q, float* act_scale, cudaStream_t stream) {
+                             int64_t K, int8_t* x_q, float* act_scale, uint8_t* x_ops, bool pdl,
+                             cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
-  const int V = (int)(K / 8);
+  const int U = (int)((K / 8 + 1) / 2);       // units of 16 inputs
   int T, vpt;
-  if (V <= 256) {
-    T = ((V + 31) / 32) * 32;
+  if (U <= 256) {
+    T = ((U + 31) / 32) * 32;
     vpt = 1;
-  } else if (V <= 2048) {
+  } else if (U <= 1024) {
     T = 256;
-    vpt = (V + 255) / 256;
+    vpt = (U + 255) / 256;
   } else {
     T = 1024;
-    vpt = (V + 1023) / 1024;
+    vpt = (U + 1023) / 1024;
   }
   int tv = 1;
   while (tv < vpt) tv <<= 1;
-  const dim3 grid((unsigned)M), block((unsigned)T);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)M, 1, 1);
+  cfg.blockDim = dim3((unsigned)T, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const uint4* gv = reinterpret_cast<const uint4*>(gain);
+  cudaError_t e;
   switch (tv) {
-    case 1: quant_act_kernel<1><<<grid, block, 0, stream>>>(xv, gv, rms_eps, (int)K, x_q, act_scale); break;
-    case 2: quant_act_kernel<2><<<grid, block, 0, stream>>>(xv, gv, rms_eps, (int)K, x_q, act_scale); break;
-    case 4: quant_act_kernel<4><<<grid, block, 0, stream>>>(xv, gv, rms_eps, (int)K, x_q, act_scale); break;
-    default: quant_act_kernel<8><<<grid, block, 0, stream>>>(xv, gv, rms_eps, (int)K, x_q, act_scale); break;
+    case 1: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<1>, xv, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, xv, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<4>, xv, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    default: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<8>, xv, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
   }
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace bitlinear

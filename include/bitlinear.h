@@ -54,12 +54,24 @@ typedef enum bitlinear_status {
     BITLINEAR_ERR_CUDA = 6,       /* a CUDA runtime call or launch failed */
     BITLINEAR_ERR_TIMEOUT = 7,    /* device: a bounded wait in a kernel ran out */
     BITLINEAR_ERR_WORKSPACE = 8,  /* workspace missing or smaller than required */
-    BITLINEAR_ERR_NONFINITE = 9   /* device: a latent weight was Inf or NaN */
+    BITLINEAR_ERR_NONFINITE = 9,  /* device: a latent weight was Inf or NaN */
+    BITLINEAR_ERR_FLAGS = 10      /* unknown bits in a flags argument */
 } bitlinear_status;
 
 /* Output element types of bitlinear_forward. */
 #define BITLINEAR_OUT_F32 0
 #define BITLINEAR_OUT_BF16 1
+
+/*
+ * Flag of bitlinear_quant_act and bitlinear_forward: launch the call's kernels
+ * as programmatic dependents of the work already on the stream, so that they
+ * start while that work finishes.  Before waiting for it, a kernel reads only
+ * the packed weights and w_scale (bitlinear_forward) or nothing at all
+ * (bitlinear_quant_act); so with this flag the packed weights and w_scale
+ * must not be written by work still in flight on the stream.  Everything else
+ * keeps plain stream order.
+ */
+#define BITLINEAR_FLAG_PDL 1u
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bitlinear_status_string(bitlinear_status status);
@@ -134,6 +146,15 @@ bitlinear_status bitlinear_pack_weights_static(const float *W, int64_t N, int64_
 /* ------------------------------------------------------------------------ */
 
 /*
+ * Bytes of the tensor-core operand form of M tokens of K int8 codes ("x_ops"):
+ * 2 * M * Kp with Kp = K rounded up to a multiple of 256.  Each code x is kept
+ * as two e4m3 planes, 16*floor((x+8)/16) and the remainder in [-8, 7], laid
+ * out in MMA fragment order; it is an internal format that only
+ * bitlinear_forward reads.
+ */
+size_t bitlinear_act_ops_bytes(int64_t M, int64_t K);
+
+/*
  * RMSNorm + per-token absmax int8 quantization ([P4-code] BitLinear.forward
  * steps 1-2 and activation_quant; [P4-eq] item 2, Q_b = 127), one token per row:
  *
@@ -153,16 +174,22 @@ bitlinear_status bitlinear_pack_weights_static(const float *W, int64_t N, int64_
  * M, K     M >= 0 (M == 0 enqueues nothing and accepts NULL buffers), 8 <= K <= 65536,
  *          K % 8 == 0.
  * x_q      [M,K] int8 out.  act_scale [M] fp32 out.
+ * x_ops    bitlinear_act_ops_bytes(M,K) bytes out (the same codes in the operand
+ *          form that bitlinear_forward consumes), or NULL.  Passing it lets
+ *          several forwards share one conversion.
+ * flags    0 or BITLINEAR_FLAG_PDL.
  */
 bitlinear_status bitlinear_quant_act(const void *x_bf16, const void *gain_bf16, float rms_eps,
                                      int64_t M, int64_t K, int8_t *x_q, float *act_scale,
-                                     void *stream);
+                                     void *x_ops, unsigned flags, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* 3. ternary contraction + dequantization                                   */
 /* ------------------------------------------------------------------------ */
 
-/* Bytes of scratch that bitlinear_forward needs for this shape (may be 0). */
+/* Bytes of scratch that bitlinear_forward needs for this shape when it is called
+ * with x_ops == NULL (it then converts x_q into the workspace first).  Called
+ * with x_ops, it needs none. */
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -174,7 +201,10 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *               output, rounded to nearest even bf16.
  *
  * x_q       [M,K] int8 (from bitlinear_quant_act).  Codes must lie in [-127,127].
- * act_scale [M] fp32.   packed [N,K/4] uint8 (from bitlinear_pack_weights).
+ *           May be NULL when x_ops is given.
+ * act_scale [M] fp32.
+ * x_ops     the same codes in operand form (bitlinear_quant_act's x_ops), or NULL.
+ * packed    [N,K/4] uint8 (from bitlinear_pack_weights).
  * w_scale   [N] fp32.
  * M, N, K   0 <= M <= 2^24 (M == 0 enqueues nothing and accepts NULL buffers),
  *           16 <= N <= 2^24, N % 16 == 0, 128 <= K <= 65536, K % 128 == 0.
@@ -182,13 +212,20 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * y         [M,N] out, fp32 or bf16.
  * acc_debug [M,N] int32 out with the raw accumulators, or NULL (for parity checks).
  * workspace >= bitlinear_forward_workspace_bytes(M,N,K) bytes of device scratch
- *           (may be NULL when that is 0).  Contents on entry do not matter.
+ *           when x_ops is NULL (else unused, may be NULL).  Contents on entry do
+ *           not matter.
+ * flags     0 or BITLINEAR_FLAG_PDL.
+ *
+ * Exactness: the kernels contract on the tensor cores with e4m3 operands; each
+ * code enters as two exact e4m3 values (see bitlinear_act_ops_bytes), and fp32
+ * partial sums are moved to int32 before they can reach 2^19, so acc is the
+ * exact integer sum.
  */
-bitlinear_status bitlinear_forward(const int8_t *x_q, const float *act_scale,
+bitlinear_status bitlinear_forward(const int8_t *x_q, const float *act_scale, const void *x_ops,
                                    const uint8_t *packed, const float *w_scale,
                                    int64_t M, int64_t N, int64_t K, int out_dtype, void *y,
                                    int32_t *acc_debug, void *workspace, size_t workspace_bytes,
-                                   void *stream);
+                                   unsigned flags, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* device error word                                                         */

@@ -2,6 +2,8 @@
 every function that include/bitlinear.h declares, sizes its buffers, and
 rejects bad arguments before touching the device."""
 import ctypes
+
+import numpy as np
 import os
 import re
 
@@ -13,7 +15,8 @@ from bitlinear_rmsnorm_token_int8_b300 import build as blbuild
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER_DIR = os.path.join(ROOT, "include")
 
-OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_WS, ERR_NF = range(10)
+(OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_WS, ERR_NF,
+ ERR_FLAGS) = range(11)
 FAKE = 1 << 20        # an aligned, never-dereferenced address
 
 
@@ -42,7 +45,7 @@ def test_library_exports_every_declared_function(L):
 
 def test_status_strings_and_version(L):
     assert L.bitlinear_abi_version() == 1
-    for s in range(10):
+    for s in range(11):
         assert L.bitlinear_status_string(s)
     assert L.bitlinear_status_string(99) == b"unknown status"
 
@@ -53,16 +56,24 @@ def test_sizes(L):
     assert L.bitlinear_pack_workspace_bytes(1, 4) >= 2048
     for M, N, K in [(1, 2560, 2560), (16, 28672, 4096), (2048, 14336, 4096)]:
         assert L.bitlinear_forward_workspace_bytes(M, N, K) >= 0
+    # operand form: two e4m3 planes, K padded to a multiple of 256
+    assert L.bitlinear_act_ops_bytes(8, 2560) == 2 * 8 * 2560
+    assert L.bitlinear_act_ops_bytes(3, 384) == 2 * 3 * 512
+    assert L.bitlinear_act_ops_bytes(-1, 384) == 0
 
 
-def _fwd(L, x=FAKE, s=FAKE, p=FAKE, w=FAKE, M=4, N=512, K=256, dt=0, y=FAKE, acc=None, ws=FAKE,
-         wsb=1 << 30):
-    return L.bitlinear_forward(x, s, p, w, M, N, K, dt, y, acc, ws, wsb, None)
+def _fwd(L, x=FAKE, s=FAKE, ops=None, p=FAKE, w=FAKE, M=4, N=512, K=256, dt=0, y=FAKE, acc=None,
+         ws=FAKE, wsb=1 << 30, flags=0):
+    return L.bitlinear_forward(x, s, ops, p, w, M, N, K, dt, y, acc, ws, wsb, flags, None)
 
 
 def test_forward_argument_errors(L):
     assert _fwd(L, x=None) == ERR_NULL
     assert _fwd(L, y=None) == ERR_NULL
+    assert _fwd(L, flags=2) == ERR_FLAGS
+    assert _fwd(L, ws=None) == ERR_WS                        # no x_ops: x_q is converted in the workspace
+    assert _fwd(L, wsb=L.bitlinear_forward_workspace_bytes(4, 512, 256) - 1) == ERR_WS
+    assert _fwd(L, ops=FAKE + 8) == ERR_ALIGN
     assert _fwd(L, M=0, x=None, y=None, s=None) == OK       # empty: nothing to touch
     assert _fwd(L, K=100) == ERR_SHAPE
     assert _fwd(L, K=0) == ERR_SHAPE
@@ -77,19 +88,24 @@ def test_forward_argument_errors(L):
     import torch
     if not torch.cuda.is_available():
         assert _fwd(L) == ERR_DEVICE
+        assert _fwd(L, x=None, ops=FAKE, ws=None, flags=1) == ERR_DEVICE   # x_ops alone suffices
 
 
 def test_quant_act_argument_errors(L):
-    q = L.bitlinear_quant_act
-    assert q(None, None, 1e-5, 4, 256, FAKE, FAKE, None) == ERR_NULL
-    assert q(None, None, 1e-5, 0, 256, None, None, None) == OK
-    assert q(FAKE, None, 1e-5, 4, 12, FAKE, FAKE, None) == ERR_SHAPE
-    assert q(FAKE, None, 1e-5, 4, 65536 + 8, FAKE, FAKE, None) == ERR_SHAPE
-    assert q(FAKE, None, 1e-5, -2, 256, FAKE, FAKE, None) == ERR_SHAPE
-    assert q(FAKE, FAKE + 2, 1e-5, 4, 256, FAKE, FAKE, None) == ERR_ALIGN
+    def q(x, g, eps, M, K, xq, sc, ops=None, flags=0):
+        return L.bitlinear_quant_act(x, g, eps, M, K, xq, sc, ops, flags, None)
+    assert q(None, None, 1e-5, 4, 256, FAKE, FAKE) == ERR_NULL
+    assert q(None, None, 1e-5, 0, 256, None, None) == OK
+    assert q(FAKE, None, 1e-5, 4, 12, FAKE, FAKE) == ERR_SHAPE
+    assert q(FAKE, None, 1e-5, 4, 65536 + 8, FAKE, FAKE) == ERR_SHAPE
+    assert q(FAKE, None, 1e-5, -2, 256, FAKE, FAKE) == ERR_SHAPE
+    assert q(FAKE, FAKE + 2, 1e-5, 4, 256, FAKE, FAKE) == ERR_ALIGN
+    assert q(FAKE, None, 1e-5, 4, 256, FAKE, FAKE, ops=FAKE + 4) == ERR_ALIGN
+    assert q(FAKE, None, 1e-5, 4, 256, FAKE, FAKE, flags=4) == ERR_FLAGS
     import torch
     if not torch.cuda.is_available():
-        assert q(FAKE, None, 1e-5, 4, 256, FAKE, FAKE, None) == ERR_DEVICE
+        assert q(FAKE, None, 1e-5, 4, 256, FAKE, FAKE) == ERR_DEVICE
+        assert q(FAKE, None, 1e-5, 4, 256, FAKE, FAKE, ops=FAKE, flags=1) == ERR_DEVICE
 
 
 def test_pack_argument_errors(L):
@@ -112,3 +128,33 @@ def test_python_binding_rejects_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         bl.bitlinear_quant_act(torch.zeros(2, 16, dtype=torch.bfloat16))
+
+
+def test_packed_layout_index_is_a_bijection_onto_the_data_bytes():
+    from bitlinear_rmsnorm_token_int8_b300 import layout
+    rng = np.random.default_rng(0)
+    for N, K in [(1, 4), (16, 512), (37, 2560), (48, 6912), (3, 516)]:
+        idx = layout.packed_index(N, K)
+        assert idx.shape == (N, K // 4)
+        assert len(np.unique(idx)) == idx.size and idx.min() >= 0 and idx.max() < layout.packed_bytes(N, K)
+        canon = rng.integers(0, 256, (N, K // 4), dtype=np.uint8)
+        tiled = layout.tiled_from_canonical(canon, K)
+        assert (layout.canonical_from_tiled(tiled, N, K) == canon).all()
+        # padding stays zero; the size matches the C ABI's
+        assert tiled.sum() == canon.astype(np.int64).sum()
+        assert layout.packed_bytes(N, K) == _lib_bytes(N, K)
+
+
+def test_packed_layout_swizzle_example():
+    # row 9 (tile 0, r = 9, r % 8 = 1), canonical byte 20 (segment 0, chunk 1, offset 4):
+    # chunk 1 ^ 1 = 0 -> offset 9*128 + 0*16 + 4
+    from bitlinear_rmsnorm_token_int8_b300 import layout
+    assert layout.packed_index(16, 512)[9, 20] == 9 * 128 + 4
+    # row 16 starts tile 1 after all segments of tile 0: K = 1024 -> 2 segments
+    assert layout.packed_index(17, 1024)[16, 0] == 2 * 2048
+    assert layout.packed_index(17, 1024)[0, 128] == 2048      # segment 1 of tile 0
+
+
+def _lib_bytes(N, K):
+    blbuild.build()
+    return bl.lib().bitlinear_packed_bytes(N, K)

@@ -13,7 +13,7 @@ import torch
 
 import bitlinear_rmsnorm_token_int8_b300 as bl
 import oracle
-from bitlinear_rmsnorm_token_int8_b300 import synth
+from bitlinear_rmsnorm_token_int8_b300 import layout, synth
 
 pytestmark = pytest.mark.gpu
 
@@ -50,9 +50,22 @@ def gpu_quant(x_bf16: torch.Tensor, gain, rms_eps):
 
 
 def gpu_pack(W: torch.Tensor, eps=1e-5):
+    """GPU packing; the packed bytes come back in the canonical [N, K/4] order."""
+    N, K = W.shape
     packed, ws, gamma = bl.bitlinear_pack_weights(W.cuda(), eps)
     torch.cuda.synchronize()
-    return packed.cpu().numpy(), ws.cpu().numpy(), np.float32(gamma.cpu().item())
+    tiled = packed.cpu().numpy()
+    # the padding of the tiled layout (rows >= N, codes >= K) holds zero codes
+    canon = layout.canonical_from_tiled(tiled, N, K)
+    mask = np.ones(tiled.size, dtype=bool)
+    mask[layout.packed_index(N, K)] = False
+    assert not tiled[: layout.packed_bytes(N, K)][mask[: layout.packed_bytes(N, K)]].any()
+    return canon, ws.cpu().numpy(), np.float32(gamma.cpu().item())
+
+
+def tiled_cuda(canon: torch.Tensor, K: int) -> torch.Tensor:
+    """Canonical [N, K/4] packed codes -> the tiled layout on the GPU."""
+    return torch.from_numpy(layout.tiled_from_canonical(canon.numpy(), K)).cuda()
 
 
 # ---------------------------------------------------------------------------
@@ -179,7 +192,8 @@ def run_forward(M, N, K, out_dtype, seed, outliers=True, gain=True):
     o_xq, o_sig = oracle.act_quant(synth.bf16_bits(x), None if g is None else synth.bf16_bits(g), RMS_EPS)
     o_packed, o_gamma, o_wq = oracle.pack_weights(W.numpy())
     return dict(x=x, y=y.cpu(), acc=acc.cpu().numpy(), xq=xq.cpu().numpy(), sc=sc.cpu().numpy(),
-                packed=packed.cpu().numpy(), gamma=np.float32(gamma.cpu().item()),
+                packed=layout.canonical_from_tiled(packed.cpu().numpy(), N, K),
+                gamma=np.float32(gamma.cpu().item()),
                 o_xq=o_xq, o_sig=o_sig, o_packed=o_packed, o_gamma=o_gamma, o_wq=o_wq)
 
 
@@ -217,6 +231,58 @@ def test_forward_matches_oracle(M, N, K, dt):
     check_output(r)
 
 
+@pytest.mark.parametrize("M,N,K,dt,pdl", [
+    (1, 2560, 2560, torch.bfloat16, True), (8, 3840, 2560, torch.bfloat16, True),
+    (16, 4096, 4096, torch.bfloat16, False), (4, 512, 256, torch.float32, True),
+    (5, 48, 384, torch.float32, True),           # K % 256 == 128: a half block at the end
+    (17, 160, 640, torch.bfloat16, True),        # two 16-token tiles, the second ragged
+    (2, 4096, 14336, torch.float32, False),      # largest K of the workloads, clusters of CTAs
+])
+def test_forward_from_quant_operands_matches_oracle(M, N, K, dt, pdl):
+    # quant_act writes the tensor-core operand form, forward consumes it (no x_q read)
+    flags = bl.FLAG_PDL if pdl else 0
+    seed = M * 7 + N + K
+    x = synth.activations(M, K, seed=seed)
+    g = synth.rms_gains(K, seed=seed + 1)
+    W = synth.latent_weights(N, K, seed=seed + 2)
+    packed, w_scale, gamma = bl.bitlinear_pack_weights(W.cuda())
+    xq, sc, ops = bl.bitlinear_quant_act(x.cuda(), g.cuda(), RMS_EPS, x_ops=True, flags=flags)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=dt, acc_debug=acc, x_ops=ops,
+                             flags=flags, K=K)
+    acc2 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y2 = bl.bitlinear_forward(xq, sc, packed, w_scale, out_dtype=dt, acc_debug=acc2, flags=flags)
+    torch.cuda.synchronize()
+    assert torch.equal(acc, acc2) and torch.equal(y, y2)     # both operand routes agree exactly
+    o_xq, o_sig = oracle.act_quant(synth.bf16_bits(x), synth.bf16_bits(g), RMS_EPS)
+    o_packed, o_gamma, o_wq = oracle.pack_weights(W.numpy())
+    r = dict(y=y.cpu(), acc=acc.cpu().numpy(), xq=xq.cpu().numpy(),
+             packed=layout.canonical_from_tiled(packed.cpu().numpy(), N, K),
+             gamma=np.float32(gamma.cpu().item()), o_xq=o_xq, o_sig=o_sig, o_packed=o_packed,
+             o_gamma=o_gamma, o_wq=o_wq)
+    check_output(r)
+
+
+def test_forward_exact_at_accumulator_extremes():
+    # every partial sum at its largest magnitude: all codes +-127 against all-(+1) / all-(-1)
+    # rows, and alternating signs so that partial sums swing between large values
+    M, N, K = 16, 64, 14336
+    xq = torch.full((M, K), 127, dtype=torch.int8)
+    xq[1] = -127
+    xq[2, ::2] = -127
+    xq[3] = torch.randint(-127, 128, (K,), dtype=torch.int8)
+    xq[4, : K // 2] = 127
+    xq[4, K // 2:] = -127
+    packed = torch.full((N, K // 4), 0x55, dtype=torch.uint8)
+    packed[1::2] = 0xAA
+    packed[2] = 0x66                       # codes 2,1,2,1: -1,+1,-1,+1 ... (byte 0b01100110)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    bl.bitlinear_forward(xq.cuda(), torch.ones(M).cuda(), tiled_cuda(packed, K), torch.ones(N).cuda(),
+                         out_dtype=torch.float32, acc_debug=acc)
+    wq = oracle.unpack_codes(packed.numpy(), K)
+    assert (acc.cpu().numpy() == oracle.ternary_matmul(xq.numpy(), wq)).all()
+
+
 def test_forward_teacher_forced_dequant_is_two_roundings():
     # y = fl(fl(acc * sigma) * w_scale): with the GPU's own sigma and gamma the fp64
     # product differs from the fp32 output by at most two binary32 roundings
@@ -237,7 +303,7 @@ def test_forward_weight_invariants_on_gpu():
     for code, sign in ((0x55, 1), (0xAA, -1), (0x00, 0)):
         packed = torch.full((32, K // 4), code, dtype=torch.uint8)
         acc = torch.empty((M, 32), dtype=torch.int32, device="cuda")
-        bl.bitlinear_forward(xq.cuda(), sc.cuda(), packed.cuda(), torch.ones(32).cuda(),
+        bl.bitlinear_forward(xq.cuda(), sc.cuda(), tiled_cuda(packed, K), torch.ones(32).cuda(),
                              out_dtype=torch.float32, acc_debug=acc)
         expect = sign * xq.to(torch.int64).sum(dim=1)
         assert (acc.cpu().to(torch.int64) == expect[:, None]).all()
@@ -251,14 +317,14 @@ def test_forward_extreme_codes_max_k():
     packed = torch.full((N, K // 4), 0x55, dtype=torch.uint8)
     packed[1::2] = 0xAA
     acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
-    bl.bitlinear_forward(xq.cuda(), torch.ones(M).cuda(), packed.cuda(), torch.ones(N).cuda(),
+    bl.bitlinear_forward(xq.cuda(), torch.ones(M).cuda(), tiled_cuda(packed, K), torch.ones(N).cuda(),
                          out_dtype=torch.float32, acc_debug=acc)
     a = acc.cpu()
     assert a[0, 0] == 127 * K and a[0, 1] == -127 * K and a[1, 0] == -127 * K
 
 
 def test_forward_empty_is_noop():
-    packed = torch.zeros((16, 32), dtype=torch.uint8, device="cuda")
+    packed = torch.zeros(bl.bitlinear_packed_bytes(16, 128), dtype=torch.uint8, device="cuda")
     y = bl.bitlinear_forward(torch.zeros((0, 128), dtype=torch.int8, device="cuda"),
                              torch.zeros(0, device="cuda"), packed, torch.ones(16, device="cuda"))
     assert y.shape == (0, 16)

@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 def _static_pack(L, W):
     N, K = W.shape
-    packed = torch.empty((N, K // 4), dtype=torch.uint8, device=W.device)
+    packed = torch.empty(bl.bitlinear_packed_bytes(N, K), dtype=torch.uint8, device=W.device)
     w_scale = torch.empty(N, dtype=torch.float32, device=W.device)
     gamma = torch.empty(4, dtype=torch.float32, device=W.device)
     fn = L.bitlinear_pack_weights_static
