@@ -9,8 +9,7 @@
 // Inference Framework", section "How the LUT Kernel Works" (2-bit code
 // 00 = 0, 01 = +1, 10 = -1, four weights per byte, int32 accumulation).
 //
-// Structure: a persistent grid (at most one CTA per SM, ~100 KB of shared
-// memory so that the next kernel's CTA fits beside it).  Work items are
+// Structure: a persistent grid, one CTA per SM.  Work items are
 // (token tile of <= 16, group of T row tiles of 16 rows = R rows, all of K);
 // CTA c takes items c, c + gridDim.x, ...  Warp 0 is the producer.  A stage is
 // SBK segments of 512 k: per row tile one bulk copy of the tile's SBK
@@ -19,7 +18,9 @@
 // NS slots signalled by mbarriers.  (Few, large requests matter: the copy
 // engine's rate is bounded per request, ~1 TB/s for 256-byte copies against
 // ~6 TB/s for 16 KB ones on this GPU, and a tensor-map box of R rows x 128
-// bytes costs about as much as R small requests.)  Warps 1..C are consumers: a segment is split in two units of 256 k, consumer w takes units
+// bytes costs about as much as R small requests.)  Warps 1..C are consumers
+// (C = 2 SBK, SBK a divisor of the segment count, at most 14 or 8 with two
+// token tiles; a stage holds one unit per consumer): a segment is split in two units of 256 k, consumer w takes units
 // w, w + C, ... of a stage, keeps a unit's activation fragments in registers
 // and runs them against all T row tiles, so the T tiles share one operand
 // load.  At the end of an item the consumers add their partial sums into
@@ -59,8 +60,6 @@ namespace bitlinear {
 namespace {
 
 constexpr uint32_t kCodeToE4M3 = 0x00B83800u;  // bytes 0x00 (code 0), 0x38 (+1), 0xB8 (-1), 0x00
-constexpr int kConsumers = 4;
-constexpr int kThreads = 32 * (1 + kConsumers);
 constexpr int kDrainUnits = 16;
 constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr int kMaxStages = 16;
@@ -107,8 +106,12 @@ __device__ __forceinline__ ItemInfo item_info(const DecodeParams& p, int item) {
   return f;
 }
 
-template <int T, int MT>
-__global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeParams p) {
+// Consumer warps: blockDim.x / 32 - 1, at most CMAX.  mma.sync needs many
+// warps in flight per SM (its issue cost is ~22 cycles per m16n8k32 e4m3 per
+// sub-partition on this GPU).
+template <int T, int MT, int CMAX>
+__global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const DecodeParams p) {
+  const int kConsumers = (int)(blockDim.x >> 5) - 1;
   extern __shared__ uint8_t smem_raw[];
   constexpr int R = T * 16;
   uint8_t* smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
@@ -231,6 +234,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodePar
             if (v != 0) atomicAdd(&s_acc[(mt * 8 + 2 * t + (c & 1)) * R + i * 16 + g + (c >> 1) * 8], v);
           }
     };
+    // Prefetch the scales of this thread's first outputs of the item: the loads
+    // complete during the contraction instead of stalling the epilogue.
+    constexpr int NPF = 4;
+    const int nout = f.Mz * R;
+    float pf_ws[NPF], pf_as[NPF];
+#pragma unroll
+    for (int j = 0; j < NPF; ++j) {
+      const int e = (int)threadIdx.x - 32 + j * 32 * kConsumers;
+      pf_ws[j] = 0.0f;
+      pf_as[j] = 0.0f;
+      if (e < nout) {
+        const int mm = e / R, rr = e - mm * R;
+        if (rr < f.ntiles * 16) {
+          pf_ws[j] = __ldg(p.w_scale + f.r0 + rr);
+          pf_as[j] = __ldg(p.act_scale + 16 * f.z + mm);
+        }
+      }
+    }
     int since_drain = 0;
     bool aborted = false;
     for (int st = 0; st < nst; ++st, ++q) {
@@ -309,19 +330,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodePar
     named_sync(1, 32 * kConsumers);
     if (aborted || *s_abort) break;
     // ---- epilogue: dequantize and store this item's outputs, clear s_acc
-    const int nout = f.Mz * R;
-    for (int e = threadIdx.x - 32; e < nout; e += 32 * kConsumers) {
+    auto store_out = [&](int e, float as, float ws) {
       const int mm = e / R, rr = e - mm * R;
       const int v = s_acc[e];
       s_acc[e] = 0;
       if (rr < f.ntiles * 16) {
         const int m = 16 * f.z + mm, n = f.r0 + rr;
         const size_t o = (size_t)m * p.N + n;
-        const float yv = __fmul_rn(__fmul_rn((float)v, p.act_scale[m]), p.w_scale[n]);
+        const float yv = __fmul_rn(__fmul_rn((float)v, as), ws);
         if (p.out_dtype == 0) reinterpret_cast<float*>(p.y)[o] = yv;
         else reinterpret_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(yv);
         if (p.acc_debug) p.acc_debug[o] = v;
       }
+    };
+#pragma unroll
+    for (int j = 0; j < NPF; ++j) {
+      const int e = (int)threadIdx.x - 32 + j * 32 * kConsumers;
+      if (e < nout) store_out(e, pf_as[j], pf_ws[j]);
+    }
+    for (int e = (int)threadIdx.x - 32 + NPF * 32 * kConsumers; e < nout; e += 32 * kConsumers) {
+      const int mm = e / R, rr = e - mm * R;
+      store_out(e, rr < f.ntiles * 16 ? __ldg(p.act_scale + 16 * f.z + mm) : 0.0f,
+                rr < f.ntiles * 16 ? __ldg(p.w_scale + f.r0 + rr) : 0.0f);
     }
     named_sync(1, 32 * kConsumers);
   }
@@ -355,33 +385,44 @@ __global__ void act_ops_from_codes_kernel(const int8_t* __restrict__ x_q, int64_
   }
 }
 
-template <int T, int MT>
+// Segments per stage: a divisor of nseg (no half-empty last stage) with two
+// units per segment = one unit per consumer warp.
+int stage_segments(int nseg, int max_sbk) {
+  int best = 0;
+  for (int d = 1; d <= max_sbk && d <= nseg; ++d)
+    if (nseg % d == 0) best = d;
+  if (best >= 3 || best == nseg) return best;
+  return nseg < max_sbk ? nseg : max_sbk;            // few divisors: accept a partial last stage
+}
+
+template <int T, int MT, int CMAX>
 cudaError_t launch_t(DecodeParams& p, int sms, bool pdl, cudaStream_t stream) {
   constexpr int R = T * 16;
   const int Mz_max = p.M < 16 ? p.M : 16;
-  int SBK = (32 * 1024) / (T * 2048 + 1024 * Mz_max);   // ~32 KB per stage
-  if (SBK > 8) SBK = 8;
-  if (SBK < 1) SBK = 1;
-  if (SBK > p.nseg) SBK = p.nseg;
+  // largest stage that leaves room for two of them in shared memory
+  int SBK = stage_segments(p.nseg, CMAX / 2);
+  while (SBK > 1 && 2L * (T * SBK * 2048 + SBK * 1024 * Mz_max) + 16 * R * 4 + 1024 > 210L * 1024)
+    SBK = stage_segments(p.nseg, SBK - 1);
+  const int C = 2 * SBK;
   p.SBK = SBK;
   p.stage_w_bytes = T * SBK * 2048;
   p.stage_bytes = p.stage_w_bytes + SBK * 1024 * Mz_max;
-  int NS = (100 * 1024) / p.stage_bytes;
+  int NS = (160 * 1024) / p.stage_bytes;
   if (NS < 2) NS = 2;
   if (NS > kMaxStages) NS = kMaxStages;
   p.NS = NS;
   const size_t smem = 128 + (size_t)NS * p.stage_bytes + 16 * R * 4 + 2 * kMaxStages * 8 + 16;
   static bool attr_set = false;   // per template instance
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<T, MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<T, MT, CMAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   const int grid = p.items < sms ? p.items : sms;
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(32 * (1 + C), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -389,7 +430,7 @@ cudaError_t launch_t(DecodeParams& p, int sms, bool pdl, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<T, MT>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<T, MT, CMAX>, p);
   count_launches(1);
   return e;
 }
@@ -441,19 +482,29 @@ cudaError_t launch_decode_mma(const uint8_t* x_ops, const float* act_scale, cons
   const int64_t work = tiles * p.ztiles;   // row tiles over all token tiles
   const int64_t Mz = M < 16 ? M : 16;
   // T row tiles per item: more tiles share each operand load (operand bytes per
-  // weight byte ~ Mz / (2 T)), fewer tiles give more items to spread over SMs.
+  // weight byte ~ Mz / (2 T)), fewer tiles give more, smaller items and so a
+  // shorter last round over the SMs.
   int T = 1;
-  if (Mz > 8) T = 2;                               // registers: two n8 token tiles
-  else if (work >= 3LL * sms) T = 4;
-  else if (work >= (3LL * sms) / 2 || Mz > 2) T = 2;
+  double best = -1.0;
+  for (int t = 1; t <= (Mz > 8 ? 2 : 4); t *= 2) {
+    const int64_t items_t = ((tiles + t - 1) / t) * p.ztiles;
+    const int64_t rounds = (items_t + sms - 1) / sms;
+    const double tail = (double)items_t / ((double)rounds * sms);
+    const double score = (items_t < sms ? (double)items_t / sms : tail) / (1.0 + 0.15 * (double)Mz / (2.0 * t));
+    if (score > best + 1e-9) {
+      best = score;
+      T = t;
+    }
+  }
   p.groups = (int)((tiles + T - 1) / T);
   const int64_t items = (int64_t)p.groups * p.ztiles;
   if (items > (1LL << 30)) return cudaErrorInvalidValue;
   p.items = (int)items;
   const bool two = M > 8;
-  if (T == 4) return launch_t<4, 1>(p, sms, pdl, stream);   // T == 4 only when Mz <= 8
-  if (T == 2) return two ? launch_t<2, 2>(p, sms, pdl, stream) : launch_t<2, 1>(p, sms, pdl, stream);
-  return two ? launch_t<1, 2>(p, sms, pdl, stream) : launch_t<1, 1>(p, sms, pdl, stream);
+  if (T == 4) return launch_t<4, 1, 14>(p, sms, pdl, stream);   // T == 4 only when Mz <= 8
+  if (T == 2)
+    return two ? launch_t<2, 2, 8>(p, sms, pdl, stream) : launch_t<2, 1, 14>(p, sms, pdl, stream);
+  return two ? launch_t<1, 2, 8>(p, sms, pdl, stream) : launch_t<1, 1, 14>(p, sms, pdl, stream);
 }
 
 }  // namespace bitlinear
