@@ -23,6 +23,13 @@
 // 2-bit weight codes (see decode_mma.cu).  The operands of one unit u of one
 // token tile are contiguous (512 Mz bytes), so one bulk copy stages a run of
 // units.  Size: 2 * M * Kp bytes.
+// Prefill layout (tcgen05 operand B, tokens in the n dimension), used when
+// M > kDecodeMaxM: two planes, each row-major [M][Kp] bytes (plane 0 = 16 h',
+// plane 1 = l', plane 1 starting at byte M * Kp), where inside every group of
+// 16 inputs the byte at position p holds input 16 g + pi(p), pi = (0, 2, 4, 6,
+// 8, 10, 12, 14, 1, 3, 5, 7, 9, 11, 13, 15): the even inputs, then the odd ones,
+// which is the order in which the prefill kernel writes decoded weights into
+// tensor memory.  Size: 2 * M * Kp bytes, as for the decode layout.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -31,6 +38,9 @@
 namespace bitlinear {
 
 constexpr int kOpsBlockK = 512;
+constexpr int64_t kDecodeMaxM = 32;      // more tokens: prefill layout and kernel
+
+__host__ __device__ __forceinline__ bool act_ops_prefill(int64_t M) { return M > kDecodeMaxM; }
 
 __host__ __device__ __forceinline__ int64_t act_ops_kpad(int64_t K) {
   return (K + kOpsBlockK - 1) / kOpsBlockK * kOpsBlockK;
@@ -63,6 +73,34 @@ __device__ __forceinline__ void write_act_ops16(uint8_t* __restrict__ ops, int64
     const int64_t off = 32 * Kp * z + (((u * 8 + 2 * j + p) * Mz + mm) * 4 + t) * 16;
     *reinterpret_cast<uint4*>(ops + off) = make_uint4(H0, H1, L0, L1);
   }
+}
+
+// Prefill-layout counterpart of write_act_ops16.
+__device__ __forceinline__ void write_act_ops16_prefill(uint8_t* __restrict__ ops, int64_t M, int64_t m,
+                                                        int64_t k, int64_t Kp, const int (&q)[16]) {
+  uint32_t H[4], L[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    H[w] = 0u;
+    L[w] = 0u;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int pos = 4 * w + b;
+      const int x = q[pos < 8 ? 2 * pos : 2 * (pos - 8) + 1];
+      const int h = (x + 8) >> 4;
+      H[w] |= e4m3_exact(16 * h) << (8 * b);
+      L[w] |= e4m3_exact(x - 16 * h) << (8 * b);
+    }
+  }
+  *reinterpret_cast<uint4*>(ops + m * Kp + k) = make_uint4(H[0], H[1], H[2], H[3]);
+  *reinterpret_cast<uint4*>(ops + (M + m) * Kp + k) = make_uint4(L[0], L[1], L[2], L[3]);
+}
+
+// Writes 16 codes in the layout that bitlinear_forward uses for M tokens.
+__device__ __forceinline__ void write_act_ops16_any(uint8_t* __restrict__ ops, int64_t M, int64_t m,
+                                                    int64_t k, int64_t Kp, const int (&q)[16]) {
+  if (act_ops_prefill(M)) write_act_ops16_prefill(ops, M, m, k, Kp, q);
+  else write_act_ops16(ops, M, m, k, Kp, q);
 }
 
 }  // namespace bitlinear

@@ -381,7 +381,7 @@ __global__ void act_ops_from_codes_kernel(const int8_t* __restrict__ x_q, int64_
         for (int j = 0; j < 8; ++j) q[8 * hv + j] = 0;
       }
     }
-    write_act_ops16(ops, M, m, k, Kp, q);
+    write_act_ops16_any(ops, M, m, k, Kp, q);
   }
 }
 

@@ -2,6 +2,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "act_ops.cuh"
 #include "internal.h"
 
 namespace bitlinear {
@@ -19,6 +20,9 @@ cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint
     x_ops = ops;
     pdl = true;   // the operand kernel just enqueued is ours: overlap with it is safe
   }
+  if (act_ops_prefill(M))
+    return launch_prefill_tc(x_ops, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
+                             dev_err, pdl, stream);
   return launch_decode_mma(x_ops, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
                            dev_err, pdl, stream);
 }

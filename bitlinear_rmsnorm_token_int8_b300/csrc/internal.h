@@ -2,6 +2,7 @@
 // Launchers validate nothing: api.cu checks every argument before calling them.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -61,6 +62,14 @@ cudaError_t launch_decode_mma(const uint8_t* x_ops, const float* act_scale, cons
                               cudaStream_t stream);
 
 int num_sms();
+
+// ---- tensor maps and the prefill contraction ---------------------------------
+bool act_planes_tensor_map(const uint8_t* ops, int64_t M, int64_t Kp, int box_rows, CUtensorMap* out);
+
+cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
+                              const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
+                              void* y, int32_t* acc_debug, int* dev_err, bool pdl,
+                              cudaStream_t stream);
 
 
 

@@ -1,0 +1,369 @@
+// Prefill contraction (many tokens) on the 5th-generation tensor cores:
+// y = dequant(x_q . W_q^T) with tcgen05.mma kind::f8f6f4, accumulators in
+// tensor memory (TMEM).
+//
+// Page "BitNet b1.58 in Production: 1-Bit LLMs and Energy Benchmarks", section
+// "The Mathematical Mechanism", items 3-4; page "BitNet 1-bit LLM Inference
+// Framework", section "How the LUT Kernel Works" (2-bit code, int32 sums).
+// The method's integer contraction is a dense matmul once M is large, so it is
+// run as one: this GPU has no int8 tcgen05 MMA, so each int8 code enters as two
+// exact e4m3 values (16 h' + l', act_ops.cuh) against e4m3 weights of -1/0/+1,
+// two MMAs per k step into one fp32 accumulator, exact while |acc| < 2^24
+// (|acc| <= 127 K <= 2^23).
+//
+// Tile: 128 weight rows (MMA M, operand A) x 256 tokens (MMA N, operand B),
+// persistent CTAs over tiles.  Roles (320 threads):
+//   warp 0      producer: per 512-k segment, eight 2 KB bulk copies of packed
+//               weights (the tile-major layout); per 128-k step, two TMA loads
+//               (3-D tensor map, 128-byte swizzle) of the token tile's two
+//               operand planes, 256 rows x 128 bytes each.
+//   warp 1      allocates TMEM (512 columns: D = 256, A = 2 x 128); one lane
+//               issues the MMAs: per 128-k step, 4 k32 steps x 2 planes.
+//   warps 2-5   decoders: thread = weight row; 2-bit codes -> e4m3 bytes by
+//               byte permutes, written to TMEM as the A operand (tcgen05.st),
+//               128 columns per segment, double buffered.
+//   warps 6-9   epilogue: tcgen05.ld of the accumulators, exact int32,
+//               y = fl(fl(acc * act_scale[m]) * w_scale[n]), stores.
+// Weights reach the tensor core through TMEM rather than shared memory: the
+// decode expands 2 bits to 8, and TMEM takes those writes without costing
+// shared-memory bandwidth.
+//
+// A row's codes are decoded word by word (16 codes): the four TMEM columns of a
+// word hold the weights of inputs (0,2,4,6), (8..14 even), (1,3,5,7), (9..15
+// odd); the prefill operand layout stores the activations in that order.
+//
+// Every mbarrier wait is bounded: on expiry the kernel records
+// BITLINEAR_ERR_TIMEOUT, all roles stop, MMAs and copies in flight are waited
+// for (bounded), and TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "act_ops.cuh"
+#include "device_util.cuh"
+#include "internal.h"
+
+namespace bitlinear {
+namespace {
+
+constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
+constexpr int kTileT = 256;                 // tokens per tile (MMA N)
+constexpr int kThreads = 320;
+constexpr int kNSX = 2;                     // operand stages (128 k each)
+constexpr int kNSW = 2;                     // weight stages (512 k each)
+constexpr int kXPlaneBytes = kTileT * 128;  // 32 KB
+constexpr int kXStageBytes = 2 * kXPlaneBytes;
+constexpr int kWStageBytes = 8 * 2048;      // 8 row tiles x one 2 KB block
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColA = 256;             // A buffers at columns 256 and 384
+constexpr uint32_t kSpin = 1u << 24;
+constexpr uint32_t kCodeToE4M3 = 0x00B83800u;  // bytes 0x00 (code 0), 0x38 (+1), 0xB8 (-1)
+
+// shared memory (after 1024-byte alignment)
+constexpr int kOffX = 0;
+constexpr int kOffW = kOffX + kNSX * kXStageBytes;
+constexpr int kOffBar = kOffW + kNSW * kWStageBytes;
+constexpr int kNumBars = 2 * kNSX + 2 * kNSW + 2 * 2 + 2 + 1;
+constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
+
+struct PrefillParams {
+  const uint8_t* packed;
+  const float* act_scale;
+  const float* w_scale;
+  void* y;
+  int32_t* acc_debug;
+  int* dev_err;
+  int M, N, K, out_dtype;
+  int nseg, ntiles_n16, nwb, ntok, tiles;
+};
+
+struct Bars {
+  uint32_t full_x, empty_x, full_w, empty_w, a_full, a_empty, d_full, d_empty, fin;
+};
+
+__device__ __forceinline__ Bars bars_at(uint32_t base) {
+  Bars b;
+  b.full_x = base;
+  b.empty_x = b.full_x + 8 * kNSX;
+  b.full_w = b.empty_x + 8 * kNSX;
+  b.empty_w = b.full_w + 8 * kNSW;
+  b.a_full = b.empty_w + 8 * kNSW;
+  b.a_empty = b.a_full + 16;
+  b.d_full = b.a_empty + 16;
+  b.d_empty = b.d_full + 8;
+  b.fin = b.d_empty + 8;
+  return b;
+}
+
+// Bounded wait; on expiry records the error and raises the CTA's abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              int* dev_err) {
+  if (mbar_wait_bounded(bar, parity, kSpin)) return true;
+  atomicCAS(dev_err, 0, kDevErrTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  const uint32_t sbase = smem_u32(smem);
+  const Bars B = bars_at(sbase + kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&xmap);
+    for (int s = 0; s < kNSX; ++s) {
+      mbar_init(B.full_x + 8 * s, 1);
+      mbar_init(B.empty_x + 8 * s, 1);
+    }
+    for (int s = 0; s < kNSW; ++s) {
+      mbar_init(B.full_w + 8 * s, 1);
+      mbar_init(B.empty_w + 8 * s, 4);            // the four decoder warps
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(B.a_full + 8 * s, 4);
+      mbar_init(B.a_empty + 8 * s, 1);
+    }
+    mbar_init(B.d_full, 1);
+    mbar_init(B.d_empty, 4);                      // the four epilogue warps
+    mbar_init(B.fin, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_launch_dependents();
+  const uint32_t tmem = s_tmem;
+  const int nseg = p.nseg;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int ws = 0, xs = 0;
+      bool waited = false;
+      for (int t = blockIdx.x; t < p.tiles && !s_abort; t += gridDim.x) {
+        const int wb = t % p.nwb, tt = t / p.nwb;
+        for (int sg = 0; sg < nseg && !s_abort; ++sg) {
+          // weights of this segment: the eight 16-row tiles of the block
+          const int wslot = ws % kNSW, wround = ws / kNSW;
+          if (wround >= 1 && !wait_or_abort(B.empty_w + 8 * wslot, (wround - 1) & 1, &s_abort, p.dev_err))
+            break;
+          const int nvalid = min(8, p.ntiles_n16 - wb * 8);
+          mbar_arrive_expect_tx(B.full_w + 8 * wslot, (uint32_t)(nvalid * 2048));
+          for (int i = 0; i < nvalid; ++i)
+            bulk_g2s(sbase + kOffW + wslot * kWStageBytes + i * 2048,
+                     p.packed + ((int64_t)(wb * 8 + i) * nseg + sg) * 2048, 2048u, B.full_w + 8 * wslot);
+          ++ws;
+          if (!waited) {                           // operands come from the previous kernel
+            pdl_wait();
+            waited = true;
+          }
+          for (int kk = 0; kk < 4; ++kk) {
+            const int xslot = xs % kNSX, xround = xs / kNSX;
+            if (xround >= 1 && !wait_or_abort(B.empty_x + 8 * xslot, (xround - 1) & 1, &s_abort, p.dev_err))
+              break;
+            mbar_arrive_expect_tx(B.full_x + 8 * xslot, (uint32_t)kXStageBytes);
+            const uint32_t dst = sbase + kOffX + xslot * kXStageBytes;
+            const int kx = (sg * 4 + kk) * 128;
+            tma_load_3d(dst, &xmap, kx, tt * kTileT, 0, B.full_x + 8 * xslot);
+            tma_load_3d(dst + kXPlaneBytes, &xmap, kx, tt * kTileT, 1, B.full_x + 8 * xslot);
+            ++xs;
+          }
+        }
+      }
+      if (!waited) pdl_wait();
+      // nothing may still be landing in shared memory when the CTA exits
+      for (int s = 0; s < kNSX && s < xs; ++s) {
+        const int last = xs - 1 - ((xs - 1 - s) % kNSX);
+        if (!mbar_wait_bounded(B.full_x + 8 * s, (last / kNSX) & 1, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+      }
+      for (int s = 0; s < kNSW && s < ws; ++s) {
+        const int last = ws - 1 - ((ws - 1 - s) % kNSW);
+        if (!mbar_wait_bounded(B.full_w + 8 * s, (last / kNSW) & 1, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = idesc_e4m3_f32(kTileW, kTileT);
+      int xs = 0, as = 0, tcount = 0;
+      for (int t = blockIdx.x; t < p.tiles && !s_abort; t += gridDim.x, ++tcount) {
+        if (tcount >= 1 && !wait_or_abort(B.d_empty, (tcount - 1) & 1, &s_abort, p.dev_err)) break;
+        tc_fence_after();
+        bool first = true;
+        for (int sg = 0; sg < nseg && !s_abort; ++sg) {
+          const int ab = as & 1;
+          if (!wait_or_abort(B.a_full + 8 * ab, (as >> 1) & 1, &s_abort, p.dev_err)) break;
+          tc_fence_after();
+          for (int kk = 0; kk < 4; ++kk) {
+            const int xslot = xs % kNSX;
+            if (!wait_or_abort(B.full_x + 8 * xslot, (xs / kNSX) & 1, &s_abort, p.dev_err)) break;
+            tc_fence_after();
+            const uint32_t xh = sbase + kOffX + xslot * kXStageBytes, xl = xh + kXPlaneBytes;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const uint32_t a = tmem + kColA + ab * 128 + kk * 32 + s * 8;
+              mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xh + 32 * s), idesc, first ? 0u : 1u);
+              mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xl + 32 * s), idesc, 1u);
+              first = false;
+            }
+            mma_commit(B.empty_x + 8 * xslot);      // frees the operand stage when these MMAs finish
+            ++xs;
+          }
+          mma_commit(B.a_empty + 8 * ab);           // frees the A buffer
+          ++as;
+        }
+        mma_commit(B.d_full);                       // accumulators complete
+      }
+      // before TMEM is freed every MMA issued here must be finished
+      mma_commit(B.fin);
+      if (!mbar_wait_bounded(B.fin, 0, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ decoders
+    const int q4 = warp & 3;                   // TMEM lane quarter of this warp
+    const int r = 32 * q4 + lane;              // weight row within the block
+    const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
+    int ws = 0, as = 0;
+    for (int t = blockIdx.x; t < p.tiles && !s_abort; t += gridDim.x) {
+      const int wb = t % p.nwb;
+      const bool valid = wb * kTileW + r < p.N;
+      for (int sg = 0; sg < nseg; ++sg) {
+        const int wslot = ws % kNSW, ab = as & 1;
+        if (!wait_or_abort(B.full_w + 8 * wslot, (ws / kNSW) & 1, &s_abort, p.dev_err)) break;
+        if (as >= 2 && !wait_or_abort(B.a_empty + 8 * ab, ((as >> 1) - 1) & 1, &s_abort, p.dev_err)) break;
+        tc_fence_after();
+        // row r of the stage: row tile r / 16, line r % 16; chunk c stored at c ^ (r % 8)
+        const uint32_t row = sbase + kOffW + wslot * kWStageBytes + (r >> 4) * 2048 + (r & 15) * 128;
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp) {        // chunk pairs: 32 TMEM columns each
+          uint32_t cols[32];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * cp + cc;
+            const uint4 v = valid ? lds128(row + (uint32_t)((c ^ (r & 7)) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t lo = wd[j] & 0x33333333u, hi = (wd[j] >> 2) & 0x33333333u;
+              uint32_t* o = cols + 16 * cc + 4 * j;
+              o[0] = __byte_perm(kCodeToE4M3, 0u, lo);          // inputs 0, 2, 4, 6
+              o[1] = __byte_perm(kCodeToE4M3, 0u, lo >> 16);    // 8, 10, 12, 14
+              o[2] = __byte_perm(kCodeToE4M3, 0u, hi);          // 1, 3, 5, 7
+              o[3] = __byte_perm(kCodeToE4M3, 0u, hi >> 16);    // 9, 11, 13, 15
+            }
+          }
+          tmem_st32(tmem + lane_addr + kColA + ab * 128 + cp * 32, cols);
+        }
+        tmem_wait_st();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.empty_w + 8 * wslot);   // weight stage read
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.a_full + 8 * ab);       // A buffer written
+        ++ws;
+        ++as;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();                                // act_scale and y follow the stream order
+    const int q4 = warp & 3;
+    const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
+    int tcount = 0;
+    for (int t = blockIdx.x; t < p.tiles && !s_abort; t += gridDim.x, ++tcount) {
+      const int wb = t % p.nwb, tt = t / p.nwb;
+      const int n = wb * kTileW + 32 * q4 + lane;
+      const bool nv = n < p.N;
+      const float wsn = nv ? __ldg(p.w_scale + n) : 0.0f;
+      if (!wait_or_abort(B.d_full, tcount & 1, &s_abort, p.dev_err)) break;
+      tc_fence_after();
+      for (int c0 = 0; c0 < kTileT; c0 += 32) {
+        const int mbase = tt * kTileT + c0;
+        const float as_lane = mbase + lane < p.M ? __ldg(p.act_scale + mbase + lane) : 0.0f;
+        uint32_t rv[32];
+        tmem_ld32(tmem + lane_addr + c0, rv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float as = __shfl_sync(0xffffffffu, as_lane, j);
+          const int m = mbase + j;
+          if (nv && m < p.M) {
+            const float a = __uint_as_float(rv[j]);         // an exact integer below 2^24
+            const size_t o = (size_t)m * p.N + n;
+            const float yv = __fmul_rn(__fmul_rn(a, as), wsn);
+            if (p.out_dtype == 0) reinterpret_cast<float*>(p.y)[o] = yv;
+            else reinterpret_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(yv);
+            if (p.acc_debug) p.acc_debug[o] = (int32_t)a;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.d_empty);   // accumulators may be overwritten
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
+                              const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
+                              void* y, int32_t* acc_debug, int* dev_err, bool pdl,
+                              cudaStream_t stream) {
+  const int64_t Kp = act_ops_kpad(K);
+  CUtensorMap xmap;
+  if (!act_planes_tensor_map(x_ops, M, Kp, kTileT, &xmap)) return cudaErrorInvalidValue;
+  PrefillParams p = {};
+  p.packed = packed;
+  p.act_scale = act_scale;
+  p.w_scale = w_scale;
+  p.y = y;
+  p.acc_debug = acc_debug;
+  p.dev_err = dev_err;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.out_dtype = out_dtype;
+  p.nseg = (int)(Kp / 512);
+  p.ntiles_n16 = (int)(N / 16);
+  p.nwb = (int)((N + kTileW - 1) / kTileW);
+  p.ntok = (int)((M + kTileT - 1) / kTileT);
+  const int64_t tiles = (int64_t)p.nwb * p.ntok;
+  if (tiles > (1LL << 30)) return cudaErrorInvalidValue;
+  p.tiles = (int)tiles;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int sms = num_sms();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.tiles < sms ? p.tiles : sms), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel, xmap, p);
+  count_launches(1);
+  return e;
+}
+
+}  // namespace bitlinear

@@ -191,14 +191,14 @@ quant_act_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gain, fl
           qr[v] = make_uint2(w0, w1);
         }
       }
-      if (x_ops) write_act_ops16(x_ops, M, row, (int64_t)u << 4, Kp, q);   // zero x -> zero code
+      if (x_ops) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, q);   // zero x -> zero code
     }
   }
   if (x_ops) {                               // zero operands of the padding up to Kp
     int z[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) z[j] = 0;
-    for (int u = U + tid; u < (int)(Kp >> 4); u += T) write_act_ops16(x_ops, M, row, (int64_t)u << 4, Kp, z);
+    for (int u = U + tid; u < (int)(Kp >> 4); u += T) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, z);
   }
 }
 

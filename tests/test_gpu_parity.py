@@ -263,6 +263,36 @@ def test_forward_from_quant_operands_matches_oracle(M, N, K, dt, pdl):
     check_output(r)
 
 
+@pytest.mark.parametrize("M,N,K,dt", [
+    (33, 48, 512, torch.float32),       # just above the decode limit; one partial weight block
+    (256, 160, 1024, torch.bfloat16),   # one full token tile
+    (300, 384, 2560, torch.float32),    # ragged second token tile
+    (512, 256, 384, torch.bfloat16),    # K % 512 == 384: a zero-padded segment tail
+    (80, 128, 14336, torch.float32),    # long K: |acc| up to 127 * 14336
+])
+def test_prefill_matches_oracle(M, N, K, dt):
+    # M > 32 tokens run on the tcgen05 kernel (weights decoded into tensor memory)
+    for pdl in (0, bl.FLAG_PDL):
+        seed = M + 3 * N + K + pdl
+        x = synth.activations(M, K, seed=seed)
+        g = synth.rms_gains(K, seed=seed + 1)
+        W = synth.latent_weights(N, K, seed=seed + 2)
+        packed, w_scale, gamma = bl.bitlinear_pack_weights(W.cuda())
+        xq, sc, ops = bl.bitlinear_quant_act(x.cuda(), g.cuda(), RMS_EPS, x_ops=True, flags=pdl)
+        acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        y = bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=dt, acc_debug=acc, x_ops=ops,
+                                 flags=pdl, K=K)
+        torch.cuda.synchronize()
+        assert bl.bitlinear_get_device_error() == 0
+        o_xq, o_sig = oracle.act_quant(synth.bf16_bits(x), synth.bf16_bits(g), RMS_EPS)
+        o_packed, o_gamma, o_wq = oracle.pack_weights(W.numpy())
+        r = dict(y=y.cpu(), acc=acc.cpu().numpy(), xq=xq.cpu().numpy(),
+                 packed=layout.canonical_from_tiled(packed.cpu().numpy(), N, K),
+                 gamma=np.float32(gamma.cpu().item()), o_xq=o_xq, o_sig=o_sig, o_packed=o_packed,
+                 o_gamma=o_gamma, o_wq=o_wq)
+        check_output(r)
+
+
 def test_forward_exact_at_accumulator_extremes():
     # every partial sum at its largest magnitude: all codes +-127 against all-(+1) / all-(-1)
     # rows, and alternating signs so that partial sums swing between large values
