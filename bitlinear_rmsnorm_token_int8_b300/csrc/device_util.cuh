@@ -300,3 +300,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 }  // namespace bitlinear
+
+namespace bitlinear {
+// 3-D TMA load multicast to the CTAs of `mask` in the cluster (same shared
+// offsets for the data and the mbarrier in each of them).
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
+      : "memory");
+}
+
+// tcgen05.commit that arrives on the mbarrier at `bar` in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+}  // namespace bitlinear

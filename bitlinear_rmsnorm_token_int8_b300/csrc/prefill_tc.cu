@@ -12,7 +12,8 @@
 // (|acc| <= 127 K <= 2^23).
 //
 // Tile: 128 weight rows (MMA M, operand A) x 256 tokens (MMA N, operand B),
-// persistent CTAs over tiles.  Roles (320 threads):
+// persistent clusters of CL = 1, 2 or 4 CTAs over tiles (TMA multicast of the
+// activation planes within a cluster, see prefill_tc_kernel).  Roles (320 threads):
 //   warp 0      producer: per 512-k segment, eight 2 KB bulk copies of packed
 //               weights (the tile-major layout); per 128-k step, two TMA loads
 //               (3-D tensor map, 128-byte swizzle) of the token tile's two
@@ -50,7 +51,7 @@ namespace {
 constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
 constexpr int kTileT = 256;                 // tokens per tile (MMA N)
 constexpr int kThreads = 320;
-constexpr int kNSX = 2;                     // operand stages (128 k each)
+constexpr int kNSX = 3;                     // operand stages (128 k each)
 constexpr int kNSW = 2;                     // weight stages (512 k each)
 constexpr int kXPlaneBytes = kTileT * 128;  // 32 KB
 constexpr int kXStageBytes = 2 * kXPlaneBytes;
@@ -105,6 +106,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return false;
 }
 
+// CL CTAs of a cluster work on CL neighbouring weight blocks of the same token
+// tile: each loads 256 / CL token rows of every operand stage and multicasts
+// them to all CL, and each one's MMA completion releases the stage in all CL,
+// so the cluster reads the activations from L2 once instead of CL times.
+template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -119,7 +125,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
     prefetch_tmap(&xmap);
     for (int s = 0; s < kNSX; ++s) {
       mbar_init(B.full_x + 8 * s, 1);
-      mbar_init(B.empty_x + 8 * s, 1);
+      mbar_init(B.empty_x + 8 * s, CL);            // one MMA commit from each CTA of the cluster
     }
     for (int s = 0; s < kNSW; ++s) {
       mbar_init(B.full_w + 8 * s, 1);
@@ -138,24 +144,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
   if (warp == 1) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();                      // peers' barriers exist before any multicast
   tc_fence_after();
   pdl_launch_dependents();
   const uint32_t tmem = s_tmem;
   const int nseg = p.nseg;
+  const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+  const int nwbg = (p.nwb + CL - 1) / CL;          // weight-block groups
+  const int ctiles = nwbg * p.ntok;
+  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int ws = 0, xs = 0;
       bool waited = false;
-      for (int t = blockIdx.x; t < p.tiles && !s_abort; t += gridDim.x) {
-        const int wb = t % p.nwb, tt = t / p.nwb;
+      for (int ct = cid; ct < ctiles && !s_abort; ct += ncl) {
+        const int wb = (ct % nwbg) * CL + rank, tt = ct / nwbg;
         for (int sg = 0; sg < nseg && !s_abort; ++sg) {
           // weights of this segment: the eight 16-row tiles of the block
           const int wslot = ws % kNSW, wround = ws / kNSW;
           if (wround >= 1 && !wait_or_abort(B.empty_w + 8 * wslot, (wround - 1) & 1, &s_abort, p.dev_err))
             break;
-          const int nvalid = min(8, p.ntiles_n16 - wb * 8);
+          const int nvalid = max(0, min(8, p.ntiles_n16 - wb * 8));
           mbar_arrive_expect_tx(B.full_w + 8 * wslot, (uint32_t)(nvalid * 2048));
           for (int i = 0; i < nvalid; ++i)
             bulk_g2s(sbase + kOffW + wslot * kWStageBytes + i * 2048,
@@ -170,10 +182,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
             if (xround >= 1 && !wait_or_abort(B.empty_x + 8 * xslot, (xround - 1) & 1, &s_abort, p.dev_err))
               break;
             mbar_arrive_expect_tx(B.full_x + 8 * xslot, (uint32_t)kXStageBytes);
-            const uint32_t dst = sbase + kOffX + xslot * kXStageBytes;
+            const uint32_t dst = sbase + kOffX + xslot * kXStageBytes + rank * (kXPlaneBytes / CL);
             const int kx = (sg * 4 + kk) * 128;
-            tma_load_3d(dst, &xmap, kx, tt * kTileT, 0, B.full_x + 8 * xslot);
-            tma_load_3d(dst + kXPlaneBytes, &xmap, kx, tt * kTileT, 1, B.full_x + 8 * xslot);
+            const int ty = tt * kTileT + rank * (kTileT / CL);
+            if (CL > 1) {
+              tma_load_3d_mc(dst, &xmap, kx, ty, 0, B.full_x + 8 * xslot, kMask);
+              tma_load_3d_mc(dst + kXPlaneBytes, &xmap, kx, ty, 1, B.full_x + 8 * xslot, kMask);
+            } else {
+              tma_load_3d(dst, &xmap, kx, ty, 0, B.full_x + 8 * xslot);
+              tma_load_3d(dst + kXPlaneBytes, &xmap, kx, ty, 1, B.full_x + 8 * xslot);
+            }
             ++xs;
           }
         }
@@ -194,7 +212,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
     if (lane == 0) {
       const uint32_t idesc = idesc_e4m3_f32(kTileW, kTileT);
       int xs = 0, as = 0, tcount = 0;
-      for (int t = blockIdx.x; t < p.tiles && !s_abort; t += gridDim.x, ++tcount) {
+      for (int ct = cid; ct < ctiles && !s_abort; ct += ncl, ++tcount) {
         if (tcount >= 1 && !wait_or_abort(B.d_empty, (tcount - 1) & 1, &s_abort, p.dev_err)) break;
         tc_fence_after();
         bool first = true;
@@ -214,7 +232,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
               mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xl + 32 * s), idesc, 1u);
               first = false;
             }
-            mma_commit(B.empty_x + 8 * xslot);      // frees the operand stage when these MMAs finish
+            if (CL > 1) mma_commit_mc(B.empty_x + 8 * xslot, kMask);   // frees the stage in every CTA
+            else mma_commit(B.empty_x + 8 * xslot);
             ++xs;
           }
           mma_commit(B.a_empty + 8 * ab);           // frees the A buffer
@@ -232,8 +251,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
     const int r = 32 * q4 + lane;              // weight row within the block
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
     int ws = 0, as = 0;
-    for (int t = blockIdx.x; t < p.tiles && !s_abort; t += gridDim.x) {
-      const int wb = t % p.nwb;
+    for (int ct = cid; ct < ctiles && !s_abort; ct += ncl) {
+      const int wb = (ct % nwbg) * CL + rank;
       const bool valid = wb * kTileW + r < p.N;
       for (int sg = 0; sg < nseg; ++sg) {
         const int wslot = ws % kNSW, ab = as & 1;
@@ -278,8 +297,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
     const int q4 = warp & 3;
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
     int tcount = 0;
-    for (int t = blockIdx.x; t < p.tiles && !s_abort; t += gridDim.x, ++tcount) {
-      const int wb = t % p.nwb, tt = t / p.nwb;
+    for (int ct = cid; ct < ctiles && !s_abort; ct += ncl, ++tcount) {
+      const int wb = (ct % nwbg) * CL + rank, tt = ct / nwbg;
       const int n = wb * kTileW + 32 * q4 + lane;
       const bool nv = n < p.N;
       const float wsn = nv ? __ldg(p.w_scale + n) : 0.0f;
@@ -312,6 +331,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();                      // no peer still sends data or arrivals here
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -323,8 +343,10 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
                               void* y, int32_t* acc_debug, int* dev_err, bool pdl,
                               cudaStream_t stream) {
   const int64_t Kp = act_ops_kpad(K);
+  const int64_t nwb = (N + kTileW - 1) / kTileW;
+  const int CL = nwb >= 2 ? 2 : 1;             // measured: 2 beats 1 and 4
   CUtensorMap xmap;
-  if (!act_planes_tensor_map(x_ops, M, Kp, kTileT, &xmap)) return cudaErrorInvalidValue;
+  if (!act_planes_tensor_map(x_ops, M, Kp, kTileT / CL, &xmap)) return cudaErrorInvalidValue;
   PrefillParams p = {};
   p.packed = packed;
   p.act_scale = act_scale;
@@ -345,23 +367,39 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
   p.tiles = (int)tiles;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (void* f : {(void*)prefill_tc_kernel<1>, (void*)prefill_tc_kernel<2>, (void*)prefill_tc_kernel<4>}) {
+      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   const int sms = num_sms();
+  const int64_t ctiles = ((nwb + CL - 1) / CL) * p.ntok;
+  int64_t clusters = sms / CL;
+  if (clusters > ctiles) clusters = ctiles;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.tiles < sms ? p.tiles : sms), 1, 1);
+  cfg.gridDim = dim3((unsigned)(clusters * CL), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = (unsigned)CL;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel, xmap, p);
+  cfg.numAttrs = na;
+  cudaError_t e;
+  if (CL == 4) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<4>, xmap, p);
+  else if (CL == 2) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<2>, xmap, p);
+  else e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<1>, xmap, p);
   count_launches(1);
   return e;
 }
