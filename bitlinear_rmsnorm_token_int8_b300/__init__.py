@@ -25,11 +25,13 @@ __all__ = [
     "BitLinearError", "lib", "library_path", "bitlinear_pack_weights", "bitlinear_quant_act",
     "bitlinear_forward", "bitlinear_get_device_error", "bitlinear_packed_bytes",
     "bitlinear_forward_workspace_bytes", "bitlinear_pack_workspace_bytes", "OUT_F32", "OUT_BF16",
-    "STATUS", "bitlinear_kernel_launches", "bitlinear_act_ops_bytes", "FLAG_PDL",
+    "STATUS", "bitlinear_kernel_launches", "bitlinear_act_ops_bytes", "FLAG_PDL", "OUT_BF16_ADD",
+    "bitlinear_block_forward", "bitlinear_block_workspace_bytes", "pack_stacked", "LAYER_FIELDS",
 ]
 
 OUT_F32 = 0
 OUT_BF16 = 1
+OUT_BF16_ADD = 2
 FLAG_PDL = 1
 STATUS = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_DTYPE", 5: "ERR_DEVICE",
           6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_WORKSPACE", 9: "ERR_NONFINITE", 10: "ERR_FLAGS"}
@@ -77,6 +79,10 @@ def lib() -> ctypes.CDLL:
         L.bitlinear_forward.restype = I
         L.bitlinear_get_device_error.argtypes = [P]
         L.bitlinear_get_device_error.restype = I
+        L.bitlinear_block_workspace_bytes.argtypes = [I64, I64, I64, I64]
+        L.bitlinear_block_workspace_bytes.restype = SZ
+        L.bitlinear_block_forward.argtypes = [P, I, I64, I64, I64, F, P, I64, P, SZ, U, P]
+        L.bitlinear_block_forward.restype = I
         _lib = L
     return _lib
 
@@ -210,6 +216,49 @@ def bitlinear_forward(x_q, act_scale: torch.Tensor, packed: torch.Tensor,
         _ptr(acc_debug), _ptr(workspace), 0 if workspace is None else workspace.numel(),
         int(flags), _stream(stream)))
     return y
+
+
+LAYER_FIELDS = ("qkv", "qkv_scale", "o", "o_scale", "gate_up", "gate_up_scale", "down", "down_scale",
+                "gain_qkv", "gain_o", "gain_gate_up", "gain_down")
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_FIELDS]
+
+
+def pack_stacked(Ws, eps: float = 1e-5, stream=None):
+    """Packs several latent matrices (each [N_i, K] fp32 CUDA, N_i % 16 == 0) as one
+    stacked projection: each keeps its own gamma.  Returns (packed, w_scale)."""
+    parts = [bitlinear_pack_weights(W, eps, stream=stream)[:2] for W in Ws]
+    return torch.cat([p for p, _ in parts]), torch.cat([s for _, s in parts])
+
+
+def bitlinear_block_workspace_bytes(M: int, H: int, NQKV: int, F: int) -> int:
+    return int(lib().bitlinear_block_workspace_bytes(M, H, NQKV, F))
+
+
+def bitlinear_block_forward(layers, x: torch.Tensor, H: int, NQKV: int, F: int, rms_eps: float = 1e-5,
+                            workspace=None, flags: int = 0, stream=None):
+    """The BitLinear stack of len(layers) transformer layers on x [M, H] bf16 (CUDA), in place.
+
+    ``layers``: dicts with the CUDA tensors named in :data:`LAYER_FIELDS` (packed weights,
+    fp32 per-row scales, bf16 RMSNorm gains).  Returns x.
+    """
+    _cuda(x, "x", torch.bfloat16)
+    M = x.shape[0]
+    arr = (_Layer * max(len(layers), 1))()
+    for i, layer in enumerate(layers):
+        for n in LAYER_FIELDS:
+            t = layer[n]
+            _cuda(t, n)
+            setattr(arr[i], n, t.data_ptr())
+    if workspace is None:
+        workspace = torch.empty(bitlinear_block_workspace_bytes(M, H, NQKV, F) + 256, dtype=torch.uint8,
+                                device=x.device)
+    _check("bitlinear_block_forward", lib().bitlinear_block_forward(
+        ctypes.cast(arr, ctypes.c_void_p), len(layers), H, NQKV, F, float(rms_eps), _ptr(x), M,
+        _ptr(workspace), workspace.numel(), int(flags), _stream(stream)))
+    return x
 
 
 def bitlinear_get_device_error(stream=None) -> int:

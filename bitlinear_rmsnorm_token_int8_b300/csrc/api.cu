@@ -170,7 +170,8 @@ bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, co
   if (M < 0 || M > (int64_t(1) << 24) || N < 16 || N % 16 != 0 || N > (int64_t(1) << 24) ||
       K < 128 || K % 128 != 0 || K > 65536)
     return BITLINEAR_ERR_SHAPE;
-  if (out_dtype != BITLINEAR_OUT_F32 && out_dtype != BITLINEAR_OUT_BF16) return BITLINEAR_ERR_DTYPE;
+  if (out_dtype != BITLINEAR_OUT_F32 && out_dtype != BITLINEAR_OUT_BF16 && out_dtype != BITLINEAR_OUT_BF16_ADD)
+    return BITLINEAR_ERR_DTYPE;
   if (flags & ~kKnownFlags) return BITLINEAR_ERR_FLAGS;
   if (M == 0) return BITLINEAR_OK;
   if (!act_scale || !packed || !w_scale || !y || (!x_q && !x_ops)) return BITLINEAR_ERR_NULL;

@@ -338,8 +338,13 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
         const int m = 16 * f.z + mm, n = f.r0 + rr;
         const size_t o = (size_t)m * p.N + n;
         const float yv = __fmul_rn(__fmul_rn((float)v, as), ws);
-        if (p.out_dtype == 0) reinterpret_cast<float*>(p.y)[o] = yv;
-        else reinterpret_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(yv);
+        if (p.out_dtype == 0) {
+          reinterpret_cast<float*>(p.y)[o] = yv;
+        } else {
+          __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o;
+          // out_dtype 2: residual add into the bf16 output, y = bf16(y + result)
+          *yb = __float2bfloat16_rn(p.out_dtype == 2 ? __fadd_rn(__bfloat162float(*yb), yv) : yv);
+        }
         if (p.acc_debug) p.acc_debug[o] = v;
       }
     };

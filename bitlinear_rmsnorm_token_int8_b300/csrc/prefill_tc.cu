@@ -318,8 +318,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
             const float a = __uint_as_float(rv[j]);         // an exact integer below 2^24
             const size_t o = (size_t)m * p.N + n;
             const float yv = __fmul_rn(__fmul_rn(a, as), wsn);
-            if (p.out_dtype == 0) reinterpret_cast<float*>(p.y)[o] = yv;
-            else reinterpret_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(yv);
+            if (p.out_dtype == 0) {
+              reinterpret_cast<float*>(p.y)[o] = yv;
+            } else {
+              __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o;
+              // out_dtype 2: residual add into the bf16 output, y = bf16(y + result)
+              *yb = __float2bfloat16_rn(p.out_dtype == 2 ? __fadd_rn(__bfloat162float(*yb), yv) : yv);
+            }
             if (p.acc_debug) p.acc_debug[o] = (int32_t)a;
           }
         }

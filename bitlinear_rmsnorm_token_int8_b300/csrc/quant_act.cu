@@ -83,11 +83,38 @@ __device__ __forceinline__ void pair_add(float& h1, float& l1, float h2, float l
 // eight bf16 ones
 __device__ __constant__ uint4 kOnes = {0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u};
 
+// Eight inputs of the gated MLP branch: h = bf16(fl(fl(max(gate, 0)^2) * up)),
+// from fp32 rows [gate (K) | up (K)], packed as bf16 pairs like an input vector.
+__device__ __forceinline__ uint4 relu2_gate8(const float* __restrict__ gu_row, int K, int v) {
+  const float4* g4 = reinterpret_cast<const float4*>(gu_row + 8 * v);
+  const float4* u4 = reinterpret_cast<const float4*>(gu_row + K + 8 * v);
+  const float4 ga = g4[0], gb = g4[1], ua = u4[0], ub = u4[1];
+  const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+  const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t pair = 0;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const float r = fmaxf(g[2 * j + b], 0.0f);
+      const float h = __fmul_rn(__fmul_rn(r, r), u[2 * j + b]);
+      pair |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(h)) << (16 * b);
+    }
+    w[j] = pair;
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // A thread owns units of 16 consecutive inputs (two 16-byte bf16 vectors), so
 // that it can store the operand form of a unit with two 16-byte stores.
+// Input: bf16 rows at x with a pitch of `ld` 16-byte vectors, or, when `glu` is
+// set, the ReLU^2-gated product of fp32 [gate | up] rows of pitch 2K (see
+// relu2_gate8).  x_q may be null (codes only in operand form).
 template <int UPT>
 __global__ void __launch_bounds__(1024)
-quant_act_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gain, float rms_eps,
+quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restrict__ glu,
+                 const uint4* __restrict__ gain, float rms_eps,
                  int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale,
                  uint8_t* __restrict__ x_ops, int64_t M) {
   pdl_wait();                                // x may be the previous kernel's output
@@ -97,7 +124,8 @@ quant_act_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gain, fl
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int T = blockDim.x;
-  const uint4* xr = x + (size_t)row * V;
+  const uint4* xr = x + (size_t)row * ld;
+  const float* gr = glu ? glu + (size_t)row * 2 * K : nullptr;
 
   uint4 xv[UPT][2];
   float amax = 0.0f;
@@ -109,7 +137,7 @@ quant_act_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gain, fl
     for (int hv = 0; hv < 2; ++hv) {
       const int v = 2 * u + hv;
       if (u < U && v < V) {
-        xv[i][hv] = __ldg(xr + v);
+        xv[i][hv] = gr ? relu2_gate8(gr, K, v) : __ldg(xr + v);
         float xf[8], gf[8];
         unpack8(xv[i][hv], xf);
         unpack8(gain ? __ldg(gain + v) : kOnes, gf);
@@ -181,7 +209,7 @@ quant_act_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gain, fl
         unpack8((gain && v < V) ? __ldg(gain + v) : kOnes, gf);
 #pragma unroll
         for (int j = 0; j < 8; ++j) q[8 * hv + j] = quant_code(__fmul_rn(xf[j], gf[j]), s, m);
-        if (v < V) {
+        if (v < V && x_q) {
           uint32_t w0 = 0, w1 = 0;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -207,6 +235,12 @@ quant_act_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gain, fl
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,
                              int64_t K, int8_t* x_q, float* act_scale, uint8_t* x_ops, bool pdl,
                              cudaStream_t stream) {
+  return launch_quant_act_ex(x, K, nullptr, gain, rms_eps, M, K, x_q, act_scale, x_ops, pdl, stream);
+}
+
+cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu, const uint16_t* gain,
+                                float rms_eps, int64_t M, int64_t K, int8_t* x_q, float* act_scale,
+                                uint8_t* x_ops, bool pdl, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
   const int U = (int)((K / 8 + 1) / 2);       // units of 16 inputs
   int T, vpt;
@@ -235,10 +269,10 @@ cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_
   const uint4* gv = reinterpret_cast<const uint4*>(gain);
   cudaError_t e;
   switch (tv) {
-    case 1: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<1>, xv, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
-    case 2: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, xv, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
-    case 4: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<4>, xv, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
-    default: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<8>, xv, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    case 1: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<1>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<4>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    default: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<8>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
   }
   count_launches(1);
   return e;

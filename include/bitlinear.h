@@ -61,6 +61,7 @@ typedef enum bitlinear_status {
 /* Output element types of bitlinear_forward. */
 #define BITLINEAR_OUT_F32 0
 #define BITLINEAR_OUT_BF16 1
+#define BITLINEAR_OUT_BF16_ADD 2   /* y is bf16 and is updated in place: y = bf16(y + result) */
 
 /*
  * Flag of bitlinear_quant_act and bitlinear_forward: launch the call's kernels
@@ -208,7 +209,8 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * w_scale   [N] fp32.
  * M, N, K   0 <= M <= 2^24 (M == 0 enqueues nothing and accepts NULL buffers),
  *           16 <= N <= 2^24, N % 16 == 0, 128 <= K <= 65536, K % 128 == 0.
- * out_dtype BITLINEAR_OUT_F32 or BITLINEAR_OUT_BF16.
+ * out_dtype BITLINEAR_OUT_F32, BITLINEAR_OUT_BF16, or BITLINEAR_OUT_BF16_ADD (residual
+ *           connection: y holds bf16 values on entry and receives bf16(fl32(y) + result)).
  * y         [M,N] out, fp32 or bf16.
  * acc_debug [M,N] int32 out with the raw accumulators, or NULL (for parity checks).
  * workspace >= bitlinear_forward_workspace_bytes(M,N,K) bytes of device scratch
@@ -226,6 +228,68 @@ bitlinear_status bitlinear_forward(const int8_t *x_q, const float *act_scale, co
                                    int64_t M, int64_t N, int64_t K, int out_dtype, void *y,
                                    int32_t *acc_debug, void *workspace, size_t workspace_bytes,
                                    unsigned flags, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* 4. the linear stack of a BitNet b1.58 transformer                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One layer's BitLinear weights (device pointers, packed by
+ * bitlinear_pack_weights) and RMSNorm gains (bf16, device).  Every BitLinear
+ * has its own RMSNorm before its activation quantization ([P4-code]
+ * BitLinear.forward).  gate_up stacks the gate rows (0..F-1) above the up rows
+ * (F..2F-1), each matrix with its own gamma in gate_up_scale.
+ */
+typedef struct bitlinear_layer {
+    const uint8_t *qkv;     const float *qkv_scale;      /* NQKV x H  */
+    const uint8_t *o;       const float *o_scale;        /* H x H     */
+    const uint8_t *gate_up; const float *gate_up_scale;  /* 2F x H    */
+    const uint8_t *down;    const float *down_scale;     /* H x F     */
+    const void *gain_qkv;   /* bf16 [H] */
+    const void *gain_o;     /* bf16 [H] */
+    const void *gain_gate_up; /* bf16 [H] */
+    const void *gain_down;  /* bf16 [F] */
+} bitlinear_layer;
+
+/* Bytes of scratch that bitlinear_block_forward needs. */
+size_t bitlinear_block_workspace_bytes(int64_t M, int64_t H, int64_t NQKV, int64_t F);
+
+/*
+ * The BitLinear projections of n_layers transformer layers on M tokens, with
+ * x [M, H] bf16 (device) as the residual stream, updated in place.  Per layer
+ * (every "BitLinear" = RMSNorm + int8 quantization + ternary contraction +
+ * dequantization, as bitlinear_quant_act + bitlinear_forward):
+ *
+ *   qkv = BitLinear_qkv(x)                  fp32 [M, NQKV], kept as bf16
+ *   q   = qkv[:, 0:H]                       attention is not part of this
+ *                                           library: the query slice stands in
+ *                                           for the attention output
+ *   x   = bf16(x + BitLinear_o(q))
+ *   g|u = BitLinear_gate_up(x)              fp32 [M, 2F]
+ *   h   = bf16(fl(fl(max(g, 0)^2) * u))     ReLU^2 gating
+ *   x   = bf16(x + BitLinear_down(h))
+ *
+ * Sources: [P4-code] BitLinear.forward (RMSNorm inside every BitLinear);
+ * [P5-block] "BitNet 1-bit LLM Inference Framework", section "A Full BitNet
+ * Transformer Block" (q/k/v/o and gate/up/down BitLinear projections, residual
+ * adds around attention and FFN).  The FFN gate here is squared ReLU, the
+ * activation of the 2B-parameter BitNet b1.58 models, in place of that block's
+ * SiLU; the block's LayerNorms are the RMSNorms of the BitLinears.
+ *
+ * layers    HOST array of n_layers structs holding device pointers.
+ * H, NQKV, F  hidden size, QKV width (>= H), FFN width; H and F multiples of 128,
+ *           NQKV a multiple of 16.
+ * rms_eps   eps of every RMSNorm (>= 0).
+ * M         tokens, 1 <= M <= 2^20.
+ * workspace >= bitlinear_block_workspace_bytes(M, H, NQKV, F) bytes of device
+ *           scratch, 256-byte aligned; contents on entry do not matter.
+ * flags     0 or BITLINEAR_FLAG_PDL (applies to the first kernel; the
+ *           following ones always overlap with their predecessor).
+ */
+bitlinear_status bitlinear_block_forward(const bitlinear_layer *layers, int n_layers, int64_t H,
+                                         int64_t NQKV, int64_t F, float rms_eps, void *x_bf16,
+                                         int64_t M, void *workspace, size_t workspace_bytes,
+                                         unsigned flags, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* device error word                                                         */

@@ -19,9 +19,15 @@ and the composition of the steps.  Each function names the passage it follows:
 * [P5-mask] same page, section "The Difference in How Computation Works"
             (mask form: y = (W==1) x - (W==-1) x).
 
-Parity pins: every function here is pinned by ``tests/test_oracle.py`` except
-``block_forward``'s attention stand-in, which is a reading, not a definition
-(see the function's docstring).
+* [P5-block] "BitNet 1-bit LLM Inference Framework", section "A Full BitNet
+            Transformer Block" (q/k/v/o and gate/up/down projections, residual
+            adds around the attention and the FFN).
+
+Parity pins: every function here is pinned by ``tests/test_oracle.py``;
+``block_layer`` is pinned only by identities (zero projections leave the
+residual stream unchanged, the gate's closed form) and by a recomputation
+with dense fp64 matmuls, its attention stand-in being a reading, not a
+definition (see the function's docstring).
 """
 from __future__ import annotations
 
@@ -263,6 +269,63 @@ def bitlinear_forward(x_bits, gain_bits, rms_eps, w_latent, eps=EPS_W):
     acc = ternary_matmul(xq, wq)
     y = dequant(acc, sigma, np.full(wq.shape[0], float(gamma)))
     return dict(x_q=xq, sigma=sigma, gamma=gamma, w_q=wq, packed=packed, acc=acc, y=y)
+
+
+# --------------------------------------------------------------------------
+# the linear stack of a transformer layer
+# --------------------------------------------------------------------------
+
+def relu2_gate_bits(gate32: np.ndarray, up32: np.ndarray) -> np.ndarray:
+    """h = bf16(fl32(fl32(max(gate, 0)^2) * up)) as bf16 bit patterns.
+
+    The FFN gate of the 2B-parameter BitNet b1.58 models is squared ReLU; the
+    block of [P5-block] uses SiLU in the same place.  gate32 and up32 are
+    binary32 values (the BitLinear outputs); each product is one binary32
+    rounding, then one rounding to bf16 (nearest even).
+    """
+    g = np.ascontiguousarray(gate32, dtype=np.float32)
+    u = np.ascontiguousarray(up32, dtype=np.float32)
+    r = np.maximum(g, np.float32(0.0))
+    h = np.multiply(np.multiply(r, r, dtype=np.float32), u, dtype=np.float32)
+    return f32_to_bf16_bits(h)
+
+
+def bitlinear_f32(x_bits, gain_bits, rms_eps, wq, w_scale):
+    """One BitLinear with its RMSNorm ([P4-code] BitLinear.forward): the fp64
+    output of :func:`dequant` rounded once to binary32."""
+    xq, sigma = act_quant(x_bits, gain_bits, rms_eps)
+    return dequant(ternary_matmul(xq, wq), sigma, w_scale).astype(np.float32)
+
+
+def block_layer(x_bits, layer: dict, rms_eps: float):
+    """One layer of the linear stack on the bf16 residual stream x [M, H].
+
+    Follows the block of [P5-block] with every projection a BitLinear (its
+    RMSNorm standing in for the block's LayerNorms):
+        q = bf16(BitLinear_qkv(x))[:, :H]    -- READING: attention is not part
+                                                of this stack, the query slice
+                                                stands in for its output
+        x = bf16(fl32(x + BitLinear_o(q)))
+        g | u = BitLinear_gate_up(x)         (fp32, gate rows then up rows)
+        h = relu2_gate_bits(g, u)
+        x = bf16(fl32(x + BitLinear_down(h)))
+    ``layer`` holds int8 ternary matrices ``qkv``, ``o``, ``gate_up``, ``down``,
+    per-row float scales ``*_scale`` and bf16 gains ``gain_*`` (bit patterns).
+    Returns the new x as bf16 bits.
+    """
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    H = x_bits.shape[1]
+    F = layer["down"].shape[1]
+    x32 = bf16_bits_to_f64(x_bits).astype(np.float32)
+    qkv = bitlinear_f32(x_bits, layer["gain_qkv"], rms_eps, layer["qkv"], layer["qkv_scale"])
+    q_bits = f32_to_bf16_bits(np.ascontiguousarray(qkv[:, :H]))
+    o = bitlinear_f32(q_bits, layer["gain_o"], rms_eps, layer["o"], layer["o_scale"])
+    x_bits = f32_to_bf16_bits(np.add(x32, o, dtype=np.float32))
+    x32 = bf16_bits_to_f64(x_bits).astype(np.float32)
+    gu = bitlinear_f32(x_bits, layer["gain_gate_up"], rms_eps, layer["gate_up"], layer["gate_up_scale"])
+    h_bits = relu2_gate_bits(gu[:, :F], gu[:, F:])
+    d = bitlinear_f32(h_bits, layer["gain_down"], rms_eps, layer["down"], layer["down_scale"])
+    return f32_to_bf16_bits(np.add(x32, d, dtype=np.float32))
 
 
 # --------------------------------------------------------------------------

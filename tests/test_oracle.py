@@ -383,3 +383,60 @@ def test_dequant_worked_example():
     ex = GOLDEN["dequant_single"]
     y = dequant(np.array([[ex["acc"]]], dtype=np.int32), np.array([ex["sigma"]]), np.array([ex["w_scale"]]))
     assert y[0, 0] == ex["y"]
+
+
+# ---------------------------------------------------------------------------
+# the linear stack (block_layer)
+# ---------------------------------------------------------------------------
+
+def _rand_layer(rng, H, NQKV, F, zero=()):
+    layer = {}
+    for name, (n, k) in {"qkv": (NQKV, H), "o": (H, H), "gate_up": (2 * F, H), "down": (H, F)}.items():
+        wq = np.zeros((n, k), np.int8) if name in zero else rng.integers(-1, 2, (n, k)).astype(np.int8)
+        layer[name] = wq
+        layer[name + "_scale"] = np.full(n, 0.01 + 0.001 * len(name))
+    for name, k in {"gain_qkv": H, "gain_o": H, "gain_gate_up": H, "gain_down": F}.items():
+        layer[name] = oracle.f32_to_bf16_bits(rng.uniform(0.5, 1.5, k).astype(np.float32))
+    return layer
+
+
+def test_relu2_gate_closed_form():
+    g = np.array([-2.0, 0.0, 1.5, 3.0, 2.0], np.float32)
+    u = np.array([5.0, 7.0, 2.0, -1.0, 0.125], np.float32)
+    h = oracle.bf16_bits_to_f64(oracle.relu2_gate_bits(g, u))
+    assert list(h) == [0.0, 0.0, 4.5, -9.0, 0.5]
+    # rounding: 1.1^2 * 1 in fp32, then to bf16 nearest
+    h2 = oracle.bf16_bits_to_f64(oracle.relu2_gate_bits(np.array([1.1], np.float32), np.array([1.0], np.float32)))
+    assert h2[0] == oracle.bf16_bits_to_f64(oracle.f32_to_bf16_bits(np.float32(1.1) * np.float32(1.1)))[0]
+
+
+def test_block_layer_zero_projections_keep_the_residual_stream():
+    rng = np.random.default_rng(5)
+    H, NQKV, F, M = 32, 48, 64, 3
+    x = oracle.f32_to_bf16_bits(rng.standard_normal((M, H)).astype(np.float32))
+    for zero in (("o", "down"), ("qkv", "o", "gate_up", "down")):
+        out = oracle.block_layer(x, _rand_layer(rng, H, NQKV, F, zero=zero), 1e-5)
+        assert (out == x).all()
+
+
+def test_block_layer_matches_dense_fp64_recomputation():
+    # the same stages with dense fp64 matmuls of dequantized operands
+    rng = np.random.default_rng(6)
+    H, NQKV, F, M = 16, 24, 32, 4
+    layer = _rand_layer(rng, H, NQKV, F)
+    x = oracle.f32_to_bf16_bits((3 * rng.standard_normal((M, H))).astype(np.float32))
+
+    def lin(xb, gain, w, ws):
+        xq, sig = oracle.act_quant(xb, gain, 1e-5)
+        return ((xq.astype(np.float64) * sig[:, None]) @ (w.astype(np.float64) * ws[:, None]).T).astype(np.float32)
+
+    x32 = oracle.bf16_bits_to_f64(x).astype(np.float32)
+    qkv = lin(x, layer["gain_qkv"], layer["qkv"], layer["qkv_scale"])
+    q = oracle.f32_to_bf16_bits(np.ascontiguousarray(qkv[:, :H]))
+    xb = oracle.f32_to_bf16_bits(x32 + lin(q, layer["gain_o"], layer["o"], layer["o_scale"]))
+    gu = lin(xb, layer["gain_gate_up"], layer["gate_up"], layer["gate_up_scale"])
+    r = np.maximum(gu[:, :F], np.float32(0))
+    h = oracle.f32_to_bf16_bits((r * r) * gu[:, F:])
+    x2 = oracle.bf16_bits_to_f64(xb).astype(np.float32)
+    expect = oracle.f32_to_bf16_bits(x2 + lin(h, layer["gain_down"], layer["down"], layer["down_scale"]))
+    assert (oracle.block_layer(x, layer, 1e-5) == expect).all()
