@@ -10,9 +10,16 @@ and projection: RMSNorm + int8 quantization of the input, then the ternary
 contraction with fused dequantization (bitlinear_quant_act + bitlinear_forward).
 Weights are packed once before timing (offline step).
 
-Metric: packed-weight GB/s (packed bytes streamed per step / step time).
+Metric: packed-weight GB/s (packed bytes streamed per step / step time).  The
+same line carries "prefill": the M = 2048 prefill of the 8B-class shapes
+(4096->14336, 14336->4096) in int8-equivalent TOPS (2 M N K / time).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode_2b|stack_2b]
+
+--workload stack_2b times bitlinear_block_forward over the 30-layer linear stack
+of the 2B-class model (hidden 2560, QKV 3840, FFN 6912, ReLU^2 gating) at
+M = 1, 8 (decode) and 512 (prefill) tokens.
 
 N > 1 runs N independent replicas (one per GPU, launched by torchrun); value is
 the aggregate over ranks and the step time the max over ranks.  The reference
@@ -247,6 +254,71 @@ def traffic_record(kernel_src: str):
     return float(r["dram_bytes_per_launch"])
 
 
+def measure_prefill(bl, synth, torch, dev, steps, warmup):
+    """M = 2048 prefill of the 8B-class shapes (4096->14336, 14336->4096): per shape one
+    graph of RMSNorm + quantization + contraction; CUDA events around `steps` replays.
+    Reports int8-equivalent TOPS (2 M N K / time) of the quant + contraction pair and
+    of the contraction alone, and the contraction's tensor-core rate against the
+    measured peak: it issues two e4m3 MMAs per int8 product, i.e. 4 M N K fp8 FLOP."""
+    wl = synth.WORKLOADS["prefill_8b_m2048"]
+    M = wl.tokens[0]
+    stream = torch.cuda.Stream(device=dev)
+    out = {"workload": "prefill_8b_m2048", "tokens": M, "shapes": []}
+    tot_ops = tot_ms = tot_fwd_ms = 0.0
+    for pi, p in enumerate(wl.projections):
+        W = synth.latent_weights_device(p.N, p.K, synth.weight_seed(wl.seed, 0, pi), dev)
+        packed, w_scale, _ = bl.bitlinear_pack_weights(W)
+        del W
+        x = synth.activations(M, p.K, synth.act_seed(wl.seed, M, p.K), outliers=True).to(dev)
+        g = synth.rms_gains(p.K, synth.gain_seed(wl.seed, 0, pi)).to(dev)
+        xq = torch.empty((M, p.K), dtype=torch.int8, device=dev)
+        sc = torch.empty(M + 4, dtype=torch.float32, device=dev)[:M]
+        ops = torch.empty(bl.bitlinear_act_ops_bytes(M, p.K), dtype=torch.uint8, device=dev)
+        y = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+        graphs = {}
+        with torch.cuda.stream(stream):
+            for kind in ("pair", "fwd"):
+                def run(kind=kind):
+                    if kind == "pair":
+                        bl.bitlinear_quant_act(x, g, RMS_EPS, x_q=xq, act_scale=sc, x_ops=ops, flags=bl.FLAG_PDL,
+                                               stream=stream)
+                    bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=torch.bfloat16, y=y, x_ops=ops,
+                                         flags=bl.FLAG_PDL, K=p.K, stream=stream)
+                run()
+                stream.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=stream):
+                    run()
+                graphs[kind] = gr
+            ms = {}
+            for kind, gr in graphs.items():
+                for _ in range(max(warmup, 3)):
+                    gr.replay()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(steps):
+                    gr.replay()
+                e1.record(stream)
+                stream.synchronize()
+                ms[kind] = e0.elapsed_time(e1) / steps
+        ops_ = 2.0 * M * p.N * p.K
+        out["shapes"].append({"K": p.K, "N": p.N, "ms": ms["pair"], "fwd_ms": ms["fwd"],
+                              "int8_equiv_tops": ops_ / (ms["pair"] * 1e9),
+                              "fwd_int8_equiv_tops": ops_ / (ms["fwd"] * 1e9)})
+        tot_ops += ops_
+        tot_ms += ms["pair"]
+        tot_fwd_ms += ms["fwd"]
+        del packed, w_scale, x, xq, ops, y, graphs
+    _, bf16_tf, src = measured_peaks()
+    fp8_peak = 2.0 * bf16_tf          # e4m3 dense rate = 2x bf16 (nominal ratio)
+    fwd_tflops = 2.0 * tot_ops / (tot_fwd_ms * 1e9)
+    out.update({"int8_equiv_tops": tot_ops / (tot_ms * 1e9), "fwd_int8_equiv_tops": tot_ops / (tot_fwd_ms * 1e9),
+                "roofline": {"bound": "tensor", "achieved": fwd_tflops, "unit": "TFLOP/s (e4m3 MMA)",
+                             "peak": fp8_peak, "frac": fwd_tflops / fp8_peak,
+                             "peak_source": f"{src} bf16 cuBLAS x 2 (nominal e4m3:bf16 ratio)"}})
+    return out
+
+
 def our_arm(args):
     import torch
     import bitlinear_rmsnorm_token_int8_b300 as bl
@@ -447,6 +519,10 @@ def our_arm(args):
                 "share_of_step": sum(fwd_ms) / ms if ms > 0 else None}
 
     # ---- CPU baseline (rank 0, N = 1 only)
+    prefill = None
+    if not args.no_prefill:
+        prefill = measure_prefill(bl, synth, torch, dev, max(3, args.steps), args.warmup)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, el, reps = oracle_sample(args.ref_seconds)
@@ -469,11 +545,74 @@ def our_arm(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "clocks": clk.summary(),
+        "prefill": prefill,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+    return 0
+
+
+def stack_arm(args):
+    """30-layer BitLinear stack (bitlinear_block_forward) at M = 1, 8 and 512 tokens."""
+    import torch
+    import bitlinear_rmsnorm_token_int8_b300 as bl
+    from bitlinear_rmsnorm_token_int8_b300 import synth
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = synth.WORKLOADS["stack_2b"]
+    H, NQKV, F = 2560, 3840, 6912
+    layers, packed_bytes = [], 0
+    for l in range(args.layers):
+        layer = {}
+        for j, (name, shapes) in enumerate({"qkv": [(NQKV, H)], "o": [(H, H)], "gate_up": [(F, H), (F, H)],
+                                            "down": [(H, F)]}.items()):
+            Ws = [synth.latent_weights_device(n, k, synth.weight_seed(wl.seed, l, 3 * j + i) + 7919 * rank, dev)
+                  for i, (n, k) in enumerate(shapes)]
+            layer[name], layer[name + "_scale"] = bl.pack_stacked(Ws)
+            packed_bytes += sum(n * k // 4 for n, k in shapes)
+            del Ws
+        for j, (name, k) in enumerate({"gain_qkv": H, "gain_o": H, "gain_gate_up": H, "gain_down": F}.items()):
+            layer[name] = synth.rms_gains(k, synth.gain_seed(wl.seed, l, j)).to(dev)
+        layers.append(layer)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    results = {}
+    for M in wl.tokens:
+        x0 = synth.activations(M, H, synth.act_seed(wl.seed, M, H), outliers=True).to(dev)
+        x = x0.clone()
+        ws = torch.empty(bl.bitlinear_block_workspace_bytes(M, H, NQKV, F) + 256, dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            bl.bitlinear_block_forward(layers, x, H, NQKV, F, RMS_EPS, workspace=ws, flags=bl.FLAG_PDL, stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                bl.bitlinear_block_forward(layers, x, H, NQKV, F, RMS_EPS, workspace=ws, flags=bl.FLAG_PDL,
+                                           stream=stream)
+            for _ in range(max(args.warmup, 3)):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            e1.record(stream)
+            stream.synchronize()
+        assert bl.bitlinear_get_device_error(stream) == 0
+        ms = e0.elapsed_time(e1) / args.steps
+        results[M] = {"ms_per_forward": ms, "tokens_per_s": M / (ms * 1e-3),
+                      "packed_gbs": packed_bytes / (ms * 1e-3) / 1e9,
+                      "int8_equiv_tops": 2.0 * M * 4 * packed_bytes / (ms * 1e9)}
+    line = {"metric": METRIC, "value": results[wl.tokens[0]]["packed_gbs"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": results[wl.tokens[0]]["ms_per_forward"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic", "config": {"workload": "stack_2b", "layers": args.layers, "hidden": H,
+                                            "qkv": NQKV, "ffn": F, "packed_bytes_per_forward": packed_bytes},
+            "per_tokens": {str(k): v for k, v in results.items()}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     return 0
 
 
@@ -486,9 +625,13 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--ref-seconds", type=float, default=12.0, help="CPU oracle seconds per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the M=2048 prefill measurement")
+    ap.add_argument("--workload", choices=["decode_2b", "stack_2b"], default="decode_2b")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.workload == "stack_2b":
+        return stack_arm(args)
     return our_arm(args)
 
 

@@ -24,12 +24,18 @@
 // token tile are contiguous (512 Mz bytes), so one bulk copy stages a run of
 // units.  Size: 2 * M * Kp bytes.
 // Prefill layout (tcgen05 operand B, tokens in the n dimension), used when
-// M > kDecodeMaxM: two planes, each row-major [M][Kp] bytes (plane 0 = 16 h',
-// plane 1 = l', plane 1 starting at byte M * Kp), where inside every group of
-// 16 inputs the byte at position p holds input 16 g + pi(p), pi = (0, 2, 4, 6,
-// 8, 10, 12, 14, 1, 3, 5, 7, 9, 11, 13, 15): the even inputs, then the odd ones,
-// which is the order in which the prefill kernel writes decoded weights into
-// tensor memory.  Size: 2 * M * Kp bytes, as for the decode layout.
+// M > kDecodeMaxM.  Tokens in tiles of 256 (Mp = M rounded up to 256), inputs
+// in blocks of 128 (Kp as above).  Per (plane, token tile, k block) one
+// contiguous 32 KB block of 256 rows x 128 bytes, blocks ordered plane-major,
+// then token tile, then k block; inside a block the 16-byte chunk c of row r
+// sits at chunk position c ^ (r % 8) (the 128-byte swizzle of the tensor core's
+// shared-memory operands, so one bulk copy stages a block as the MMA reads it),
+// and inside every group of 16 inputs the byte at position p holds input
+// 16 g + pi(p), pi = (0, 2, 4, 6, 8, 10, 12, 14, 1, 3, 5, 7, 9, 11, 13, 15): the
+// even inputs, then the odd ones, the order in which the prefill kernel writes
+// decoded weights into tensor memory.  Plane 0 = 16 h', plane 1 = l'.  Rows of
+// the last tile past M are never read into a stored output and are left as
+// they are.  Size: 2 * Mp * Kp bytes.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -75,6 +81,14 @@ __device__ __forceinline__ void write_act_ops16(uint8_t* __restrict__ ops, int64
   }
 }
 
+__host__ __device__ __forceinline__ int64_t act_ops_mpad(int64_t M) { return (M + 255) / 256 * 256; }
+
+// Byte offset of the 16-byte chunk holding inputs [k, k + 16) of token m, plane 0.
+__device__ __forceinline__ int64_t prefill_ops_offset(int64_t m, int64_t k, int64_t Kp) {
+  const int64_t tt = m >> 8, r = m & 255, kb = k >> 7, c = (k >> 4) & 7;
+  return ((tt * (Kp >> 7) + kb) << 15) + (r << 7) + ((c ^ (r & 7)) << 4);
+}
+
 // Prefill-layout counterpart of write_act_ops16.
 __device__ __forceinline__ void write_act_ops16_prefill(uint8_t* __restrict__ ops, int64_t M, int64_t m,
                                                         int64_t k, int64_t Kp, const int (&q)[16]) {
@@ -92,8 +106,9 @@ __device__ __forceinline__ void write_act_ops16_prefill(uint8_t* __restrict__ op
       L[w] |= e4m3_exact(x - 16 * h) << (8 * b);
     }
   }
-  *reinterpret_cast<uint4*>(ops + m * Kp + k) = make_uint4(H[0], H[1], H[2], H[3]);
-  *reinterpret_cast<uint4*>(ops + (M + m) * Kp + k) = make_uint4(L[0], L[1], L[2], L[3]);
+  const int64_t off = prefill_ops_offset(m, k, Kp);
+  *reinterpret_cast<uint4*>(ops + off) = make_uint4(H[0], H[1], H[2], H[3]);
+  *reinterpret_cast<uint4*>(ops + act_ops_mpad(M) * Kp + off) = make_uint4(L[0], L[1], L[2], L[3]);
 }
 
 // Writes 16 codes in the layout that bitlinear_forward uses for M tokens.

@@ -442,7 +442,9 @@ cudaError_t launch_t(DecodeParams& p, int sms, bool pdl, cudaStream_t stream) {
 
 }  // namespace
 
-size_t act_ops_bytes(int64_t M, int64_t K) { return (size_t)(2 * M * act_ops_kpad(K)); }
+size_t act_ops_bytes(int64_t M, int64_t K) {
+  return (size_t)(2 * (act_ops_prefill(M) ? act_ops_mpad(M) : M) * act_ops_kpad(K));
+}
 
 cudaError_t launch_act_ops_from_codes(const int8_t* x_q, int64_t M, int64_t K, uint8_t* ops,
                                       bool pdl, cudaStream_t stream) {

@@ -321,3 +321,15 @@ __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 }  // namespace bitlinear
+
+namespace bitlinear {
+// Bulk copy global -> shared memory multicast to the CTAs of `mask` (same
+// shared offsets for the data and the mbarrier in each of them).
+__device__ __forceinline__ void bulk_g2s_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                            uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "h"(mask)
+      : "memory");
+}
+}  // namespace bitlinear

@@ -70,7 +70,6 @@ cudaError_t launch_decode_mma(const uint8_t* x_ops, const float* act_scale, cons
 int num_sms();
 
 // ---- tensor maps and the prefill contraction ---------------------------------
-bool act_planes_tensor_map(const uint8_t* ops, int64_t M, int64_t Kp, int box_rows, CUtensorMap* out);
 
 cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
                               const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,

@@ -15,16 +15,22 @@
 // persistent clusters of CL = 1, 2 or 4 CTAs over tiles (TMA multicast of the
 // activation planes within a cluster, see prefill_tc_kernel).  Roles (320 threads):
 //   warp 0      producer: per 512-k segment, eight 2 KB bulk copies of packed
-//               weights (the tile-major layout); per 128-k step, two TMA loads
-//               (3-D tensor map, 128-byte swizzle) of the token tile's two
-//               operand planes, 256 rows x 128 bytes each.
+//               weights (the tile-major layout); per 128-k step, one bulk copy
+//               per operand plane of the token tile's 32 KB block, already in
+//               the swizzled layout the MMA reads (act_ops.cuh).  Copies are
+//               few and large because the copy engine's cost is per request,
+//               and per 128-byte row for tensor-map boxes.
 //   warp 1      allocates TMEM (512 columns: D = 256, A = 2 x 128); one lane
 //               issues the MMAs: per 128-k step, 4 k32 steps x 2 planes.
 //   warps 2-5   decoders: thread = weight row; 2-bit codes -> e4m3 bytes by
 //               byte permutes, written to TMEM as the A operand (tcgen05.st),
 //               128 columns per segment, double buffered.
-//   warps 6-9   epilogue: tcgen05.ld of the accumulators, exact int32,
-//               y = fl(fl(acc * act_scale[m]) * w_scale[n]), stores.
+//   warps 6-13  epilogue: two warps per TMEM lane quarter, each taking half of
+//               the tile's tokens; tcgen05.ld of the accumulators (one chunk of
+//               32 tokens ahead), exact int32, y = fl(fl(acc * act_scale[m]) *
+//               w_scale[n]), stores.  The scales are loaded before the wait for
+//               the accumulators: the epilogue is the part of a tile that the
+//               MMAs of the next tile wait for.
 // Weights reach the tensor core through TMEM rather than shared memory: the
 // decode expands 2 bits to 8, and TMEM takes those writes without costing
 // shared-memory bandwidth.
@@ -50,7 +56,7 @@ namespace {
 
 constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
 constexpr int kTileT = 256;                 // tokens per tile (MMA N)
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kNSX = 3;                     // operand stages (128 k each)
 constexpr int kNSW = 2;                     // weight stages (512 k each)
 constexpr int kXPlaneBytes = kTileT * 128;  // 32 KB
@@ -70,6 +76,8 @@ constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
 
 struct PrefillParams {
   const uint8_t* packed;
+  const uint8_t* x_ops;
+  int64_t plane_bytes;            // Mp * Kp
   const float* act_scale;
   const float* w_scale;
   void* y;
@@ -107,12 +115,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 }
 
 // CL CTAs of a cluster work on CL neighbouring weight blocks of the same token
-// tile: each loads 256 / CL token rows of every operand stage and multicasts
+// tile: each copies 256 / CL token rows of every operand stage and multicasts
 // them to all CL, and each one's MMA completion releases the stage in all CL,
 // so the cluster reads the activations from L2 once instead of CL times.
 template <int CL>
-__global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   __shared__ uint32_t s_tmem;
@@ -122,7 +129,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    prefetch_tmap(&xmap);
     for (int s = 0; s < kNSX; ++s) {
       mbar_init(B.full_x + 8 * s, 1);
       mbar_init(B.empty_x + 8 * s, CL);            // one MMA commit from each CTA of the cluster
@@ -136,7 +142,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
       mbar_init(B.a_empty + 8 * s, 1);
     }
     mbar_init(B.d_full, 1);
-    mbar_init(B.d_empty, 4);                      // the four epilogue warps
+    mbar_init(B.d_empty, 8);                      // the eight epilogue warps
     mbar_init(B.fin, 1);
     s_abort = 0;
     fence_mbar_init();
@@ -182,15 +188,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
             if (xround >= 1 && !wait_or_abort(B.empty_x + 8 * xslot, (xround - 1) & 1, &s_abort, p.dev_err))
               break;
             mbar_arrive_expect_tx(B.full_x + 8 * xslot, (uint32_t)kXStageBytes);
-            const uint32_t dst = sbase + kOffX + xslot * kXStageBytes + rank * (kXPlaneBytes / CL);
-            const int kx = (sg * 4 + kk) * 128;
-            const int ty = tt * kTileT + rank * (kTileT / CL);
+            const uint32_t part = kXPlaneBytes / CL;            // this CTA's rows of the block
+            const uint32_t dst = sbase + kOffX + xslot * kXStageBytes + rank * part;
+            const uint8_t* src = p.x_ops + (((int64_t)tt * (nseg * 4) + sg * 4 + kk) << 15) + rank * part;
             if (CL > 1) {
-              tma_load_3d_mc(dst, &xmap, kx, ty, 0, B.full_x + 8 * xslot, kMask);
-              tma_load_3d_mc(dst + kXPlaneBytes, &xmap, kx, ty, 1, B.full_x + 8 * xslot, kMask);
+              bulk_g2s_mc(dst, src, part, B.full_x + 8 * xslot, kMask);
+              bulk_g2s_mc(dst + kXPlaneBytes, src + p.plane_bytes, part, B.full_x + 8 * xslot, kMask);
             } else {
-              tma_load_3d(dst, &xmap, kx, ty, 0, B.full_x + 8 * xslot);
-              tma_load_3d(dst + kXPlaneBytes, &xmap, kx, ty, 1, B.full_x + 8 * xslot);
+              bulk_g2s(dst, src, part, B.full_x + 8 * xslot);
+              bulk_g2s(dst + kXPlaneBytes, src + p.plane_bytes, part, B.full_x + 8 * xslot);
             }
             ++xs;
           }
@@ -295,38 +301,63 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillParams 
     // ------------------------------------------------------------ epilogue
     pdl_wait();                                // act_scale and y follow the stream order
     const int q4 = warp & 3;
+    const int half = (warp - 6) >> 2;          // tokens [128 half, 128 half + 128) of the tile
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
+    constexpr int kChunks = kTileT / 2 / 32;   // 4 chunks of 32 tokens
+    const int out_mode = p.out_dtype;
     int tcount = 0;
     for (int ct = cid; ct < ctiles && !s_abort; ct += ncl, ++tcount) {
       const int wb = (ct % nwbg) * CL + rank, tt = ct / nwbg;
       const int n = wb * kTileW + 32 * q4 + lane;
       const bool nv = n < p.N;
       const float wsn = nv ? __ldg(p.w_scale + n) : 0.0f;
+      const int m0 = tt * kTileT + half * (kTileT / 2);
+      float as_lane[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int m = m0 + 32 * c + lane;
+        as_lane[c] = m < p.M ? __ldg(p.act_scale + m) : 0.0f;
+      }
       if (!wait_or_abort(B.d_full, tcount & 1, &s_abort, p.dev_err)) break;
       tc_fence_after();
-      for (int c0 = 0; c0 < kTileT; c0 += 32) {
-        const int mbase = tt * kTileT + c0;
-        const float as_lane = mbase + lane < p.M ? __ldg(p.act_scale + mbase + lane) : 0.0f;
-        uint32_t rv[32];
-        tmem_ld32(tmem + lane_addr + c0, rv);
-        tmem_wait_ld();
+      uint32_t rv[2][32];
+      tmem_ld32(tmem + lane_addr + half * (kTileT / 2), rv[0]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float as = __shfl_sync(0xffffffffu, as_lane, j);
-          const int m = mbase + j;
-          if (nv && m < p.M) {
-            const float a = __uint_as_float(rv[j]);         // an exact integer below 2^24
-            const size_t o = (size_t)m * p.N + n;
-            const float yv = __fmul_rn(__fmul_rn(a, as), wsn);
-            if (p.out_dtype == 0) {
-              reinterpret_cast<float*>(p.y)[o] = yv;
-            } else {
-              __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o;
-              // out_dtype 2: residual add into the bf16 output, y = bf16(y + result)
-              *yb = __float2bfloat16_rn(p.out_dtype == 2 ? __fadd_rn(__bfloat162float(*yb), yv) : yv);
-            }
-            if (p.acc_debug) p.acc_debug[o] = (int32_t)a;
+      for (int c = 0; c < kChunks; ++c) {
+        tmem_wait_ld();
+        if (c + 1 < kChunks) tmem_ld32(tmem + lane_addr + half * (kTileT / 2) + 32 * (c + 1), rv[(c + 1) & 1]);
+        const int mbase = m0 + 32 * c;
+        const int jmax = nv ? min(32, p.M - mbase) : 0;       // tokens of this chunk that exist
+        const size_t o0 = (size_t)mbase * p.N + n;
+        if (out_mode == 1) {                                 // bf16
+          __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float as = __shfl_sync(0xffffffffu, as_lane[c], j);
+            if (j < jmax) yb[(size_t)j * p.N] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(__uint_as_float(rv[c & 1][j]), as), wsn));
           }
+        } else if (out_mode == 0) {                          // fp32
+          float* yf = reinterpret_cast<float*>(p.y) + o0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float as = __shfl_sync(0xffffffffu, as_lane[c], j);
+            if (j < jmax) yf[(size_t)j * p.N] = __fmul_rn(__fmul_rn(__uint_as_float(rv[c & 1][j]), as), wsn);
+          }
+        } else {                                             // bf16 residual add
+          __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float as = __shfl_sync(0xffffffffu, as_lane[c], j);
+            if (j < jmax) {
+              const float yv = __fmul_rn(__fmul_rn(__uint_as_float(rv[c & 1][j]), as), wsn);
+              yb[(size_t)j * p.N] = __float2bfloat16_rn(__fadd_rn(__bfloat162float(yb[(size_t)j * p.N]), yv));
+            }
+          }
+        }
+        if (p.acc_debug) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < jmax) p.acc_debug[o0 + (size_t)j * p.N] = (int32_t)__uint_as_float(rv[c & 1][j]);
         }
       }
       tc_fence_before();
@@ -350,10 +381,10 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
   const int64_t Kp = act_ops_kpad(K);
   const int64_t nwb = (N + kTileW - 1) / kTileW;
   const int CL = nwb >= 2 ? 2 : 1;             // measured: 2 beats 1 and 4
-  CUtensorMap xmap;
-  if (!act_planes_tensor_map(x_ops, M, Kp, kTileT / CL, &xmap)) return cudaErrorInvalidValue;
   PrefillParams p = {};
   p.packed = packed;
+  p.x_ops = x_ops;
+  p.plane_bytes = act_ops_mpad(M) * Kp;
   p.act_scale = act_scale;
   p.w_scale = w_scale;
   p.y = y;
@@ -402,9 +433,9 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
   cfg.attrs = attr;
   cfg.numAttrs = na;
   cudaError_t e;
-  if (CL == 4) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<4>, xmap, p);
-  else if (CL == 2) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<2>, xmap, p);
-  else e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<1>, xmap, p);
+  if (CL == 4) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<4>, p);
+  else if (CL == 2) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<2>, p);
+  else e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<1>, p);
   count_launches(1);
   return e;
 }

@@ -60,6 +60,7 @@ def test_sizes(L):
     assert L.bitlinear_act_ops_bytes(8, 2560) == 2 * 8 * 2560
     assert L.bitlinear_act_ops_bytes(3, 384) == 2 * 3 * 512
     assert L.bitlinear_act_ops_bytes(-1, 384) == 0
+    assert L.bitlinear_act_ops_bytes(33, 384) == 2 * 256 * 512      # prefill layout: tokens padded to 256
 
 
 def _fwd(L, x=FAKE, s=FAKE, ops=None, p=FAKE, w=FAKE, M=4, N=512, K=256, dt=0, y=FAKE, acc=None,
