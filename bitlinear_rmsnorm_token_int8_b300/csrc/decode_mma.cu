@@ -76,6 +76,7 @@ struct DecodeParams {
   int groups, ztiles, items;
   int nseg;                       // 512-wide k segments (K rounded up)
   int SBK, NS, stage_w_bytes, stage_bytes;
+  int bres_bytes;                 // > 0: all operands resident in shared memory (one copy)
 };
 
 __device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -115,9 +116,11 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
   extern __shared__ uint8_t smem_raw[];
   constexpr int R = T * 16;
   uint8_t* smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
-  int* s_acc = reinterpret_cast<int*>(smem + p.NS * p.stage_bytes);             // [16][R]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_acc + 16 * R);                  // full[16], empty[16]
-  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages);
+  const uint32_t bres = smem_u32(smem) + p.NS * p.stage_bytes;                   // resident operands
+  int* s_acc = reinterpret_cast<int*>(smem + p.NS * p.stage_bytes + p.bres_bytes);  // [16][R]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_acc + 16 * R);           // full[16], empty[16], bfull
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 1);
+  const uint32_t bfull = smem_u32(bars + 2 * kMaxStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ring = smem_u32(smem);
@@ -129,6 +132,7 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kConsumers);
     }
+    mbar_init(bfull, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -145,6 +149,7 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
     bool waited = false;
     int deferred = 0;               // stages whose operand copy waits for the previous kernel
     auto issue_ops = [&](int qq) {
+      if (p.bres_bytes) return;                     // operands are staged once, resident
       const int item = blockIdx.x + (qq / nst) * gridDim.x, st = qq % nst;
       const ItemInfo f = item_info<T>(p, item);
       const int seg0 = st * p.SBK, nsg = min(p.SBK, p.nseg - seg0);
@@ -161,6 +166,10 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
           if (!waited) {            // ring full: from here on the operands are needed
             pdl_wait();
             waited = true;
+            if (p.bres_bytes) {
+              mbar_arrive_expect_tx(bfull, (uint32_t)p.bres_bytes);
+              bulk_g2s(bres, p.x_ops, (uint32_t)p.bres_bytes, bfull);
+            }
             for (int d = 0; d < deferred; ++d) issue_ops(q - deferred + d);
             deferred = 0;
           }
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
           }
         }
         const int seg0 = st * p.SBK, nsg = min(p.SBK, p.nseg - seg0);
-        const uint32_t tx = (uint32_t)(f.ntiles * nsg * 2048 + nsg * 1024 * f.Mz);
+        const uint32_t tx = (uint32_t)(f.ntiles * nsg * 2048 + (p.bres_bytes ? 0 : nsg * 1024 * f.Mz));
         mbar_arrive_expect_tx(full0 + 8 * slot, tx);
         const uint32_t dst = ring + slot * p.stage_bytes;
         const int tile0 = f.r0 >> 4;
@@ -184,8 +193,13 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
     }
     if (!waited) {
       pdl_wait();
+      if (p.bres_bytes) {
+        mbar_arrive_expect_tx(bfull, (uint32_t)p.bres_bytes);
+        bulk_g2s(bres, p.x_ops, (uint32_t)p.bres_bytes, bfull);
+      }
       for (int d = 0; d < deferred; ++d) issue_ops(q - deferred + d);
     }
+    if (p.bres_bytes && !mbar_wait_bounded(bfull, 0, kSpinLimit)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
     // No copy may still be landing in shared memory when the CTA exits: wait
     // (bounded) for the last phase of every slot that was used.
     const int used = q < p.NS ? q : p.NS;
@@ -204,6 +218,12 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
   // all four apart, NA = 2 separates the planes.
   constexpr int NA = (T >= 4 || MT == 2) ? 2 : 4;
   pdl_wait();                        // act_scale and y follow the stream order
+  if (p.bres_bytes && !mbar_wait_bounded(bfull, 0, kSpinLimit)) {
+    if (lane == 0) {
+      atomicCAS(p.dev_err, 0, kDevErrTimeout);
+      *s_abort = 1;
+    }
+  }
   const int cw = warp - 1;
   const int g = lane >> 2, t = lane & 3;
   int q = 0;
@@ -266,7 +286,8 @@ __global__ void __launch_bounds__(32 * (1 + CMAX), 1) decode_mma_kernel(const De
       }
       const int seg0 = st * p.SBK, nsg = min(p.SBK, p.nseg - seg0);
       const uint32_t wbase = ring + slot * p.stage_bytes;
-      const uint32_t bbase = wbase + p.stage_w_bytes;
+      // operands of unit u of the item: resident block, or this stage's copy
+      const uint32_t bbase = p.bres_bytes ? bres + (uint32_t)(2 * seg0) * 512 * f.Mz : wbase + p.stage_w_bytes;
       for (int cu = cw; cu < 2 * nsg; cu += kConsumers) {
         const int sg = cu >> 1, h = cu & 1;
         uint4 xb[8][MT];
@@ -404,19 +425,38 @@ template <int T, int MT, int CMAX>
 cudaError_t launch_t(DecodeParams& p, int sms, bool pdl, cudaStream_t stream) {
   constexpr int R = T * 16;
   const int Mz_max = p.M < 16 ? p.M : 16;
-  // largest stage that leaves room for two of them in shared memory
-  int SBK = stage_segments(p.nseg, CMAX / 2);
-  while (SBK > 1 && 2L * (T * SBK * 2048 + SBK * 1024 * Mz_max) + 16 * R * 4 + 1024 > 210L * 1024)
-    SBK = stage_segments(p.nseg, SBK - 1);
-  const int C = 2 * SBK;
+  const int64_t Kp = (int64_t)p.nseg * 512;
+  // With one token tile and operands of at most 112 KB, the operands are copied
+  // once and stay resident; stages then carry weights only (~32 KB each).
+  const int64_t bres_need = 2 * (int64_t)Mz_max * Kp;
+  const bool resident = p.ztiles == 1 && bres_need <= 112 * 1024;
+  p.bres_bytes = resident ? (int)bres_need : 0;
+  int SBK;
+  if (resident) {
+    SBK = stage_segments(p.nseg, 16 / T > 1 ? 16 / T : 1);
+  } else {
+    // largest stage that leaves room for two of them in shared memory
+    SBK = stage_segments(p.nseg, CMAX / 2);
+    while (SBK > 1 && 2L * (T * SBK * 2048 + SBK * 1024 * Mz_max) + 16 * R * 4 + 1024 > 210L * 1024)
+      SBK = stage_segments(p.nseg, SBK - 1);
+  }
+  // consumers: one or more whole units each (a unit = 256 k of a segment)
+  int C = 2 * SBK;
+  while (C > CMAX) {
+    int d = CMAX;
+    while (d > 1 && (2 * SBK) % d != 0) --d;
+    C = d >= 2 ? d : CMAX;
+    break;
+  }
   p.SBK = SBK;
   p.stage_w_bytes = T * SBK * 2048;
-  p.stage_bytes = p.stage_w_bytes + SBK * 1024 * Mz_max;
-  int NS = (160 * 1024) / p.stage_bytes;
+  p.stage_bytes = p.stage_w_bytes + (resident ? 0 : SBK * 1024 * Mz_max);
+  int NS = (int)((200L * 1024 - p.bres_bytes - 16 * R * 4) / p.stage_bytes);
   if (NS < 2) NS = 2;
   if (NS > kMaxStages) NS = kMaxStages;
   p.NS = NS;
-  const size_t smem = 128 + (size_t)NS * p.stage_bytes + 16 * R * 4 + 2 * kMaxStages * 8 + 16;
+  const size_t smem = 128 + (size_t)NS * p.stage_bytes + p.bres_bytes + 16 * R * 4 + (2 * kMaxStages + 1) * 8 + 16;
+  if (smem > 220 * 1024) return cudaErrorInvalidValue;
   static bool attr_set = false;   // per template instance
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<T, MT, CMAX>,
@@ -486,29 +526,15 @@ cudaError_t launch_decode_mma(const uint8_t* x_ops, const float* act_scale, cons
   p.ztiles = (int)((M + 15) / 16);
   p.nseg = (int)(act_ops_kpad(K) / 512);
   const int64_t tiles = N / 16;
-  const int64_t work = tiles * p.ztiles;   // row tiles over all token tiles
-  const int64_t Mz = M < 16 ? M : 16;
-  // T row tiles per item: more tiles share each operand load (operand bytes per
-  // weight byte ~ Mz / (2 T)), fewer tiles give more, smaller items and so a
-  // shorter last round over the SMs.
-  int T = 1;
-  double best = -1.0;
-  for (int t = 1; t <= (Mz > 8 ? 2 : 4); t *= 2) {
-    const int64_t items_t = ((tiles + t - 1) / t) * p.ztiles;
-    const int64_t rounds = (items_t + sms - 1) / sms;
-    const double tail = (double)items_t / ((double)rounds * sms);
-    const double score = (items_t < sms ? (double)items_t / sms : tail) / (1.0 + 0.15 * (double)Mz / (2.0 * t));
-    if (score > best + 1e-9) {
-      best = score;
-      T = t;
-    }
-  }
+  // T row tiles per item.  Measured on the decode shapes (N = 2560 .. 28672,
+  // M = 1 .. 16): T = 2 beats T = 1 (more per-item synchronisation and epilogue
+  // work per weight byte) and T = 4 (fewer items than SMs on small N).
+  const int T = tiles >= 2 ? 2 : 1;
   p.groups = (int)((tiles + T - 1) / T);
   const int64_t items = (int64_t)p.groups * p.ztiles;
   if (items > (1LL << 30)) return cudaErrorInvalidValue;
   p.items = (int)items;
   const bool two = M > 8;
-  if (T == 4) return launch_t<4, 1, 14>(p, sms, pdl, stream);   // T == 4 only when Mz <= 8
   if (T == 2)
     return two ? launch_t<2, 2, 8>(p, sms, pdl, stream) : launch_t<2, 1, 14>(p, sms, pdl, stream);
   return two ? launch_t<1, 2, 8>(p, sms, pdl, stream) : launch_t<1, 1, 14>(p, sms, pdl, stream);

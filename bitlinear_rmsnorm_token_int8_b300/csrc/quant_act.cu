@@ -244,15 +244,17 @@ cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu,
   if (M == 0) return cudaSuccess;
   const int U = (int)((K / 8 + 1) / 2);       // units of 16 inputs
   int T, vpt;
+  // Few rows (decode): each row is one CTA's serial chain, so spread it over up
+  // to 1024 threads.  Many rows: 256-thread CTAs keep many rows in flight.
   if (U <= 256) {
     T = ((U + 31) / 32) * 32;
     vpt = 1;
-  } else if (U <= 1024) {
+  } else if (M < num_sms() || U > 1024) {
+    T = U <= 1024 ? ((U + 31) / 32) * 32 : 1024;
+    vpt = (U + T - 1) / T;
+  } else {
     T = 256;
     vpt = (U + 255) / 256;
-  } else {
-    T = 1024;
-    vpt = (U + 1023) / 1024;
   }
   int tv = 1;
   while (tv < vpt) tv <<= 1;
