@@ -117,13 +117,26 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
                  const uint4* __restrict__ gain, float rms_eps,
                  int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale,
                  uint8_t* __restrict__ x_ops, int64_t M) {
-  pdl_wait();                                // x may be the previous kernel's output
-  pdl_launch_dependents();
   const int V = K >> 3;                      // 16-byte vectors per row
   const int U = (V + 1) >> 1;                // units of 16 inputs
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int T = blockDim.x;
+  // the RMSNorm gain is not written by earlier kernels: with few units per thread
+  // (the short-M launch) load it before waiting; longer rows reload it in place
+  constexpr bool kPreGain = UPT <= 2;
+  uint4 gv_[kPreGain ? UPT : 1][2];
+  if constexpr (kPreGain) {
+#pragma unroll
+    for (int i = 0; i < UPT; ++i)
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        const int v = 2 * (tid + i * T) + hv;
+        gv_[i][hv] = (gain && tid + i * T < U && v < V) ? __ldg(gain + v) : kOnes;
+      }
+  }
+  pdl_wait();                                // x may be the previous kernel's output
+  pdl_launch_dependents();
   const uint4* xr = x + (size_t)row * ld;
   const float* gr = glu ? glu + (size_t)row * 2 * K : nullptr;
 
@@ -140,7 +153,8 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
         xv[i][hv] = gr ? relu2_gate8(gr, K, v) : __ldg(xr + v);
         float xf[8], gf[8];
         unpack8(xv[i][hv], xf);
-        unpack8(gain ? __ldg(gain + v) : kOnes, gf);
+        if constexpr (kPreGain) unpack8(gv_[i][hv], gf);
+        else unpack8(gain ? __ldg(gain + v) : kOnes, gf);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           amax = fmaxf(amax, fabsf(__fmul_rn(xf[j], gf[j])));
@@ -206,7 +220,8 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
         float xf[8], gf[8];
         unpack8(xv[i][hv], xf);
         const int v = 2 * u + hv;
-        unpack8((gain && v < V) ? __ldg(gain + v) : kOnes, gf);
+        if constexpr (kPreGain) unpack8(gv_[i][hv], gf);
+        else unpack8((gain && v < V) ? __ldg(gain + v) : kOnes, gf);
 #pragma unroll
         for (int j = 0; j < 8; ++j) q[8 * hv + j] = quant_code(__fmul_rn(xf[j], gf[j]), s, m);
         if (v < V && x_q) {
