@@ -519,10 +519,10 @@ def our_arm(args):
     # ---- roofline of the dominant kernel (the contraction)
     hbm, bf16_tf, peak_src = measured_peaks()
     achieved = sum(alg_bytes_fwd) / (sum(fwd_ms) * 1e-3) / 1e9
-    traffic = traffic_record(os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc", "decode_mma.cu"))
+    traffic = traffic_record(os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc", "decode_tc.cu"))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic, "peak_source": peak_src,
-                "kernel": "decode_mma_kernel (bitlinear_forward: ternary contraction + dequant)",
+                "kernel": "decode_tc_kernel (bitlinear_forward: ternary contraction + dequant, tcgen05)",
                 "timing": "CUDA events around K replays of a graph of the 30 layers' launches per (M, projection)",
                 "alg_bytes_per_launch": sum(alg_bytes_fwd) / len(alg_bytes_fwd),
                 "avg_launch_us": sum(fwd_ms) / len(fwd_ms) * 1e3,

@@ -333,3 +333,10 @@ __device__ __forceinline__ void bulk_g2s_mc(uint32_t dst, const void* src, uint3
       : "memory");
 }
 }  // namespace bitlinear
+
+namespace bitlinear {
+// Atomic add into a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ void red_add_shared_cluster(uint32_t addr, int v) {
+  asm volatile("red.shared::cluster.add.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+}  // namespace bitlinear

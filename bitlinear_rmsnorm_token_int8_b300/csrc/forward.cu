@@ -23,8 +23,8 @@ cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint
   if (act_ops_prefill(M))
     return launch_prefill_tc(x_ops, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
                              dev_err, pdl, stream);
-  return launch_decode_mma(x_ops, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
-                           dev_err, pdl, stream);
+  return launch_decode_tc(x_ops, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
+                          dev_err, pdl, stream);
 }
 
 }  // namespace bitlinear

@@ -62,10 +62,24 @@ cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint
                            int64_t K, int out_dtype, void* y, int32_t* acc_debug, void* workspace,
                            int* dev_err, bool pdl, cudaStream_t stream);
 
-cudaError_t launch_decode_mma(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
-                              const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
-                              void* y, int32_t* acc_debug, int* dev_err, bool pdl,
-                              cudaStream_t stream);
+// Decode contraction (M <= kDecodeMaxM) on tcgen05: launch plan and launcher.
+struct DecodePlan {
+  int Mt;            // tokens padded to 8 (MMA n = 2 Mt: both operand planes)
+  int nseg;          // 512-wide K segments
+  int ntile;         // 128-row weight tiles
+  int S;             // K slices = CTAs per cluster
+  int G;             // segments per pipeline stage
+  int NS;            // pipeline stages
+  int stage_bytes;   // shared bytes per stage (weights, then operands)
+  int64_t smem;      // dynamic shared memory per CTA
+};
+DecodePlan decode_plan(int64_t M, int64_t N, int64_t K, int sms);
+bool decode_plan_ok(const DecodePlan& pl);
+
+cudaError_t launch_decode_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
+                             const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
+                             void* y, int32_t* acc_debug, int* dev_err, bool pdl,
+                             cudaStream_t stream);
 
 int num_sms();
 

@@ -114,6 +114,23 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return false;
 }
 
+// Warp-collective form for the warps whose next step is a tcgen05 load or
+// store (.sync.aligned): every lane takes the same branch.
+__device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                   int* dev_err) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kSpin));
+  if (!ok && (threadIdx.x & 31) == 0) {
+    atomicCAS(dev_err, 0, kDevErrTimeout);
+    *abort_flag = 1;
+  }
+  __syncwarp();
+  return ok;
+}
+
+__device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
+  return __any_sync(0xffffffffu, *abort_flag != 0);
+}
+
 // CL CTAs of a cluster work on CL neighbouring weight blocks of the same token
 // tile: each copies 256 / CL token rows of every operand stage and multicasts
 // them to all CL, and each one's MMA completion releases the stage in all CL,
@@ -257,13 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     const int r = 32 * q4 + lane;              // weight row within the block
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
     int ws = 0, as = 0;
-    for (int ct = cid; ct < ctiles && !s_abort; ct += ncl) {
+    for (int ct = cid; ct < ctiles && !warp_aborted(&s_abort); ct += ncl) {
       const int wb = (ct % nwbg) * CL + rank;
       const bool valid = wb * kTileW + r < p.N;
       for (int sg = 0; sg < nseg; ++sg) {
         const int wslot = ws % kNSW, ab = as & 1;
-        if (!wait_or_abort(B.full_w + 8 * wslot, (ws / kNSW) & 1, &s_abort, p.dev_err)) break;
-        if (as >= 2 && !wait_or_abort(B.a_empty + 8 * ab, ((as >> 1) - 1) & 1, &s_abort, p.dev_err)) break;
+        if (!warp_wait_or_abort(B.full_w + 8 * wslot, (ws / kNSW) & 1, &s_abort, p.dev_err)) break;
+        if (as >= 2 && !warp_wait_or_abort(B.a_empty + 8 * ab, ((as >> 1) - 1) & 1, &s_abort, p.dev_err)) break;
         tc_fence_after();
         // row r of the stage: row tile r / 16, line r % 16; chunk c stored at c ^ (r % 8)
         const uint32_t row = sbase + kOffW + wslot * kWStageBytes + (r >> 4) * 2048 + (r & 15) * 128;
@@ -306,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     constexpr int kChunks = kTileT / 2 / 32;   // 4 chunks of 32 tokens
     const int out_mode = p.out_dtype;
     int tcount = 0;
-    for (int ct = cid; ct < ctiles && !s_abort; ct += ncl, ++tcount) {
+    for (int ct = cid; ct < ctiles && !warp_aborted(&s_abort); ct += ncl, ++tcount) {
       const int wb = (ct % nwbg) * CL + rank, tt = ct / nwbg;
       const int n = wb * kTileW + 32 * q4 + lane;
       const bool nv = n < p.N;
@@ -318,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
         const int m = m0 + 32 * c + lane;
         as_lane[c] = m < p.M ? __ldg(p.act_scale + m) : 0.0f;
       }
-      if (!wait_or_abort(B.d_full, tcount & 1, &s_abort, p.dev_err)) break;
+      if (!warp_wait_or_abort(B.d_full, tcount & 1, &s_abort, p.dev_err)) break;
       tc_fence_after();
       uint32_t rv[2][32];
       tmem_ld32(tmem + lane_addr + half * (kTileT / 2), rv[0]);

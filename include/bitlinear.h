@@ -148,10 +148,12 @@ bitlinear_status bitlinear_pack_weights_static(const float *W, int64_t N, int64_
 
 /*
  * Bytes of the tensor-core operand form of M tokens of K int8 codes ("x_ops"):
- * 2 * M * Kp with Kp = K rounded up to a multiple of 256.  Each code x is kept
- * as two e4m3 planes, 16*floor((x+8)/16) and the remainder in [-8, 7], laid
- * out in MMA fragment order; it is an internal format that only
- * bitlinear_forward reads.
+ * 2 * Mt * Kp with Kp = K rounded up to a multiple of 512 and Mt = M rounded up
+ * to a multiple of 8 for M <= 32 (decode), to a multiple of 256 above (prefill).
+ * Each code x is kept as two e4m3 planes, 16*floor((x+8)/16) and the remainder
+ * in [-8, 7], in the swizzled shared-memory layout the tensor cores read; it is
+ * an internal format that only bitlinear_forward reads, and it depends on M, so
+ * x_ops written for M tokens is only valid for a forward with the same M.
  */
 size_t bitlinear_act_ops_bytes(int64_t M, int64_t K);
 

@@ -56,9 +56,11 @@ def test_sizes(L):
     assert L.bitlinear_pack_workspace_bytes(1, 4) >= 2048
     for M, N, K in [(1, 2560, 2560), (16, 28672, 4096), (2048, 14336, 4096)]:
         assert L.bitlinear_forward_workspace_bytes(M, N, K) >= 0
-    # operand form: two e4m3 planes, K padded to a multiple of 256
+    # operand form: two e4m3 planes, K padded to a multiple of 512
     assert L.bitlinear_act_ops_bytes(8, 2560) == 2 * 8 * 2560
-    assert L.bitlinear_act_ops_bytes(3, 384) == 2 * 3 * 512
+    assert L.bitlinear_act_ops_bytes(3, 384) == 2 * 8 * 512        # decode layout: tokens padded to 8
+    assert L.bitlinear_act_ops_bytes(17, 1024) == 2 * 24 * 1024
+    assert L.bitlinear_act_ops_bytes(32, 640) == 2 * 32 * 1024
     assert L.bitlinear_act_ops_bytes(-1, 384) == 0
     assert L.bitlinear_act_ops_bytes(33, 384) == 2 * 256 * 512      # prefill layout: tokens padded to 256
 

@@ -225,10 +225,19 @@ def check_output(r, ts=None, ns=None):
     (1, 16, 128, torch.float32), (3, 48, 384, torch.bfloat16), (8, 272, 640, torch.float32),
     (17, 160, 1024, torch.bfloat16), (16, 2560, 2560, torch.float32), (40, 256, 6912, torch.bfloat16),
     (129, 384, 512, torch.float32),
+    (24, 272, 4608, torch.bfloat16),     # three 8-token groups, K split over a cluster of CTAs
+    (32, 400, 1536, torch.float32),      # the largest decode M; a partial 128-row tile
 ])
 def test_forward_matches_oracle(M, N, K, dt):
     r = run_forward(M, N, K, dt, seed=M * 131 + N + K)
     check_output(r)
+
+
+def test_forward_every_decode_m():
+    # every token count the decode kernel takes (1..32: 8-token groups and their ragged ends)
+    for M in range(1, 33):
+        r = run_forward(M, 144, 1152, torch.float32, seed=9000 + M)
+        check_output(r)
 
 
 @pytest.mark.parametrize("M,N,K,dt,pdl", [
