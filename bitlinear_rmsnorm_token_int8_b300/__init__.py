@@ -13,6 +13,8 @@ section "The Mathematical Mechanism", items 1-4):
 * :func:`bitlinear_pack_weights`  absmean ternarization + 2-bit packing
 * :func:`bitlinear_quant_act`     RMSNorm + per-token absmax int8 quantization
 * :func:`bitlinear_forward`       exact int32 ternary contraction + dequantization
+* :func:`bitlinear_linear_forward` the whole layer: the two above in one call
+* :func:`bitlinear_block_forward`  the BitLinear stack of transformer layers
 """
 from __future__ import annotations
 
@@ -27,6 +29,7 @@ __all__ = [
     "bitlinear_forward_workspace_bytes", "bitlinear_pack_workspace_bytes", "OUT_F32", "OUT_BF16",
     "STATUS", "bitlinear_kernel_launches", "bitlinear_act_ops_bytes", "FLAG_PDL", "OUT_BF16_ADD",
     "bitlinear_block_forward", "bitlinear_block_workspace_bytes", "pack_stacked", "LAYER_FIELDS",
+    "bitlinear_linear_forward", "bitlinear_linear_workspace_bytes",
 ]
 
 OUT_F32 = 0
@@ -83,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.bitlinear_block_workspace_bytes.restype = SZ
         L.bitlinear_block_forward.argtypes = [P, I, I64, I64, I64, F, P, I64, P, SZ, U, P]
         L.bitlinear_block_forward.restype = I
+        L.bitlinear_linear_workspace_bytes.argtypes = [I64, I64, I64]
+        L.bitlinear_linear_workspace_bytes.restype = SZ
+        L.bitlinear_linear_forward.argtypes = [P, P, F, P, P, I64, I64, I64, I, P, P, P, P, P, SZ, U, P]
+        L.bitlinear_linear_forward.restype = I
         _lib = L
     return _lib
 
@@ -215,6 +222,48 @@ def bitlinear_forward(x_q, act_scale: torch.Tensor, packed: torch.Tensor,
         _ptr(x_q), _ptr(act_scale), _ptr(x_ops), _ptr(packed), _ptr(w_scale), M, N, K, code, _ptr(y),
         _ptr(acc_debug), _ptr(workspace), 0 if workspace is None else workspace.numel(),
         int(flags), _stream(stream)))
+    return y
+
+
+def bitlinear_linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().bitlinear_linear_workspace_bytes(M, N, K))
+
+
+def bitlinear_linear_forward(x: torch.Tensor, gain, rms_eps: float, packed: torch.Tensor,
+                             w_scale: torch.Tensor, out_dtype=torch.bfloat16, y=None, x_q=None,
+                             act_scale=None, acc_debug=None, workspace=None, flags: int = 0,
+                             residual: bool = False, stream=None):
+    """The BitLinear layer: y [M,N] = dequant(quant(RMSNorm(x)) . W_q^T) from bf16 x [M,K] (CUDA).
+
+    ``gain``: RMSNorm weight (bf16 [K]) or None; ``rms_eps < 0`` skips RMSNorm.  ``x_q``
+    (int8 [M,K]) and ``act_scale`` (fp32 [M]) receive the codes and scales when given.
+    ``residual``: y (bf16) holds the residual on entry and receives y + result.
+    """
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(packed, "packed", torch.uint8)
+    _cuda(w_scale, "w_scale", torch.float32)
+    if gain is not None:
+        _cuda(gain, "gain", torch.bfloat16)
+    M, K = x.shape
+    N = w_scale.shape[0]
+    if packed.numel() < bitlinear_packed_bytes(N, K):
+        raise ValueError("packed is smaller than bitlinear_packed_bytes(N, K)")
+    code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(out_dtype)
+    if code is None:
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    if residual:
+        if y is None or out_dtype != torch.bfloat16:
+            raise ValueError("residual needs a bf16 y")
+        code = OUT_BF16_ADD
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if workspace is None:
+        need = bitlinear_linear_workspace_bytes(M, N, K)
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device) if need else None
+    _check("bitlinear_linear_forward", lib().bitlinear_linear_forward(
+        _ptr(x), _ptr(gain), float(rms_eps), _ptr(packed), _ptr(w_scale), M, N, K, code, _ptr(y),
+        _ptr(x_q), _ptr(act_scale), _ptr(acc_debug), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), int(flags), _stream(stream)))
     return y
 
 

@@ -192,6 +192,51 @@ bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, co
                                   static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// Workspace of bitlinear_linear_forward when it runs as quantization + contraction:
+// [0, ops) the operand form of the codes, [ops, ops + 4 M) the per-token scales.
+size_t linear_ops_bytes(int64_t M, int64_t K) { return (act_ops_bytes(M, K) + 255) / 256 * 256; }
+size_t linear_split_bytes(int64_t M, int64_t K) { return linear_ops_bytes(M, K) + (size_t)(4 * M + 255) / 256 * 256; }
+}  // namespace
+
+size_t bitlinear_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 16 || N % 16 != 0 || K < 128 || K % 128 != 0 || K > 65536) return 0;
+  return linear_split_bytes(M, K);
+}
+
+bitlinear_status bitlinear_linear_forward(const void* x_bf16, const void* gain_bf16, float rms_eps,
+                                          const uint8_t* packed, const float* w_scale, int64_t M,
+                                          int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
+                                          float* act_scale, int32_t* acc_debug, void* workspace,
+                                          size_t workspace_bytes, unsigned flags, void* stream) {
+  if (M < 0 || M > (int64_t(1) << 24) || N < 16 || N % 16 != 0 || N > (int64_t(1) << 24) ||
+      K < 128 || K % 128 != 0 || K > 65536)
+    return BITLINEAR_ERR_SHAPE;
+  if (out_dtype != BITLINEAR_OUT_F32 && out_dtype != BITLINEAR_OUT_BF16 && out_dtype != BITLINEAR_OUT_BF16_ADD)
+    return BITLINEAR_ERR_DTYPE;
+  if (flags & ~kKnownFlags) return BITLINEAR_ERR_FLAGS;
+  if (M == 0) return BITLINEAR_OK;
+  if (!x_bf16 || !packed || !w_scale || !y) return BITLINEAR_ERR_NULL;
+  if (!aligned16(x_bf16) || (gain_bf16 && !aligned16(gain_bf16)) || !aligned16(packed) ||
+      !aligned16(w_scale) || !aligned16(y) || (x_q && !aligned16(x_q)) || (act_scale && !aligned16(act_scale)) ||
+      (acc_debug && !aligned16(acc_debug)))
+    return BITLINEAR_ERR_ALIGN;
+  if (!workspace || workspace_bytes < linear_split_bytes(M, K)) return BITLINEAR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return BITLINEAR_ERR_ALIGN;
+  const DeviceState* dev = current_device();
+  if (!dev) return BITLINEAR_ERR_DEVICE;
+  const bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ops = static_cast<uint8_t*>(workspace);
+  float* scale = act_scale ? act_scale : reinterpret_cast<float*>(ops + linear_ops_bytes(M, K));
+  cudaError_t e = launch_quant_act(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
+                                   rms_eps, M, K, x_q, scale, ops, pdl, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  // the contraction follows a kernel of this library: overlapping with it is safe
+  return from_cuda(launch_forward(nullptr, scale, ops, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
+                                  nullptr, dev->err_word, true, s));
+}
+
 bitlinear_status bitlinear_get_device_error(void* stream) {
   const DeviceState* dev = current_device();
   if (!dev) return BITLINEAR_ERR_DEVICE;

@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
       for (int m = 0; m < Mt; ++m) {
         if (m < p.M) {
           const int v = S > 1 ? acc[m] + s_red[m * kRows + r] : acc[m];
-          const float as = __ldg(p.act_scale + m);
+          const float as = __ldcg(p.act_scale + m);
           const size_t o = (size_t)m * p.N + n;
           const float yv = __fmul_rn(__fmul_rn((float)v, as), wsn);
           if (p.out_dtype == 0) {

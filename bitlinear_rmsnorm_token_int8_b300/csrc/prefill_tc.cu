@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
         const int m = m0 + 32 * c + lane;
-        as_lane[c] = m < p.M ? __ldg(p.act_scale + m) : 0.0f;
+        as_lane[c] = m < p.M ? __ldcg(p.act_scale + m) : 0.0f;
       }
       if (!warp_wait_or_abort(B.d_full, tcount & 1, &s_abort, p.dev_err)) break;
       tc_fence_after();

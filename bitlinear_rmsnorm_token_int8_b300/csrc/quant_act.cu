@@ -88,7 +88,7 @@ __device__ __constant__ uint4 kOnes = {0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x
 __device__ __forceinline__ uint4 relu2_gate8(const float* __restrict__ gu_row, int K, int v) {
   const float4* g4 = reinterpret_cast<const float4*>(gu_row + 8 * v);
   const float4* u4 = reinterpret_cast<const float4*>(gu_row + K + 8 * v);
-  const float4 ga = g4[0], gb = g4[1], ua = u4[0], ub = u4[1];
+  const float4 ga = __ldcg(g4), gb = __ldcg(g4 + 1), ua = __ldcg(u4), ub = __ldcg(u4 + 1);
   const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
   const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
   uint32_t w[4];
@@ -150,7 +150,7 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
     for (int hv = 0; hv < 2; ++hv) {
       const int v = 2 * u + hv;
       if (u < U && v < V) {
-        xv[i][hv] = gr ? relu2_gate8(gr, K, v) : __ldg(xr + v);
+        xv[i][hv] = gr ? relu2_gate8(gr, K, v) : __ldcg(xr + v);
         float xf[8], gf[8];
         unpack8(xv[i][hv], xf);
         if constexpr (kPreGain) unpack8(gv_[i][hv], gf);

@@ -221,15 +221,42 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * flags     0 or BITLINEAR_FLAG_PDL.
  *
  * Exactness: the kernels contract on the tensor cores with e4m3 operands; each
- * code enters as two exact e4m3 values (see bitlinear_act_ops_bytes), and fp32
- * partial sums are moved to int32 before they can reach 2^19, so acc is the
- * exact integer sum.
+ * code enters as two exact e4m3 values (see bitlinear_act_ops_bytes) and every
+ * fp32 accumulator stays an integer below 2^24 in magnitude (at most 128 K <= 2^23),
+ * so acc is the exact integer sum.
  */
 bitlinear_status bitlinear_forward(const int8_t *x_q, const float *act_scale, const void *x_ops,
                                    const uint8_t *packed, const float *w_scale,
                                    int64_t M, int64_t N, int64_t K, int out_dtype, void *y,
                                    int32_t *acc_debug, void *workspace, size_t workspace_bytes,
                                    unsigned flags, void *stream);
+
+/* Bytes of scratch that bitlinear_linear_forward needs: the operand form of the
+ * codes and the per-token scales. */
+size_t bitlinear_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * The whole BitLinear layer in one call ([P4-code] BitLinear.forward: RMSNorm,
+ * activation_quant, the ternary product and the rescale; [P1-impl]
+ * bitlinear_forward(x, W_packed, s)): enqueues bitlinear_quant_act into the
+ * workspace, then bitlinear_forward on its operand form, the second launch
+ * overlapping the first (programmatic dependent launch).  Results equal those of
+ * the two calls.
+ *
+ * x_bf16, gain_bf16, rms_eps  as bitlinear_quant_act (K % 128 == 0 here).
+ * packed, w_scale, M, N, K, out_dtype, y, acc_debug  as bitlinear_forward.
+ * x_q       [M,K] int8 out, or NULL.  act_scale [M] fp32 out, or NULL (then kept
+ *           in the workspace).
+ * workspace >= bitlinear_linear_workspace_bytes(M,N,K) bytes of device scratch.
+ *           Contents on entry do not matter.
+ * flags     0 or BITLINEAR_FLAG_PDL (the first launch may overlap the work
+ *           already on the stream).
+ */
+bitlinear_status bitlinear_linear_forward(const void *x_bf16, const void *gain_bf16, float rms_eps,
+                                          const uint8_t *packed, const float *w_scale, int64_t M,
+                                          int64_t N, int64_t K, int out_dtype, void *y, int8_t *x_q,
+                                          float *act_scale, int32_t *acc_debug, void *workspace,
+                                          size_t workspace_bytes, unsigned flags, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* 4. the linear stack of a BitNet b1.58 transformer                         */

@@ -111,6 +111,33 @@ def test_quant_act_argument_errors(L):
         assert q(FAKE, None, 1e-5, 4, 256, FAKE, FAKE, ops=FAKE, flags=1) == ERR_DEVICE
 
 
+def test_linear_forward_argument_errors(L):
+    def lf(x=FAKE, g=None, p=FAKE, w=FAKE, M=4, N=512, K=256, dt=1, y=FAKE, xq=None, sc=None, acc=None,
+           ws=None, wsb=0, flags=0):
+        return L.bitlinear_linear_forward(x, g, 1e-5, p, w, M, N, K, dt, y, xq, sc, acc, ws, wsb, flags, None)
+    assert lf(x=None) == ERR_NULL
+    assert lf(p=None) == ERR_NULL
+    assert lf(M=0, x=None, p=None, w=None, y=None) == OK
+    assert lf(K=200) == ERR_SHAPE                   # the contraction needs K % 128 == 0
+    assert lf(N=24) == ERR_SHAPE
+    assert lf(M=-1) == ERR_SHAPE
+    assert lf(dt=5) == ERR_DTYPE
+    assert lf(flags=8) == ERR_FLAGS
+    assert lf(g=FAKE + 2) == ERR_ALIGN
+    assert lf(xq=FAKE + 8) == ERR_ALIGN
+    # quantization into the workspace (operand form + scales), then the contraction
+    assert L.bitlinear_linear_workspace_bytes(1, 2560, 2560) >= L.bitlinear_act_ops_bytes(1, 2560) + 4
+    need = L.bitlinear_linear_workspace_bytes(64, 512, 256)
+    assert need >= L.bitlinear_act_ops_bytes(64, 256) + 4 * 64
+    assert lf(M=64) == ERR_WS
+    assert lf(M=64, ws=FAKE, wsb=need - 1) == ERR_WS
+    assert lf(M=64, ws=FAKE + 4, wsb=need) == ERR_ALIGN
+    assert lf() == ERR_WS
+    import torch
+    if not torch.cuda.is_available():
+        assert lf(M=64, ws=FAKE, wsb=need) == ERR_DEVICE
+
+
 def test_pack_argument_errors(L):
     p = L.bitlinear_pack_weights
     ws = L.bitlinear_pack_workspace_bytes(8, 8)
