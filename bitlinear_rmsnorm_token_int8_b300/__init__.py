@@ -276,8 +276,13 @@ class _Layer(ctypes.Structure):
 
 
 def pack_stacked(Ws, eps: float = 1e-5, stream=None):
-    """Packs several latent matrices (each [N_i, K] fp32 CUDA, N_i % 16 == 0) as one
-    stacked projection: each keeps its own gamma.  Returns (packed, w_scale)."""
+    """Packs several latent matrices (each [N_i, K] fp32 CUDA) as one stacked projection:
+    each keeps its own gamma.  Every N_i but the last must be a multiple of 128 (the
+    packed layout's row tile), the last a multiple of 16.  Returns (packed, w_scale)."""
+    for i, W in enumerate(Ws):
+        n = W.shape[0]
+        if n % 16 != 0 or (i + 1 < len(Ws) and n % 128 != 0):
+            raise ValueError("stacked matrices need N_i % 128 == 0 (the last: N % 16 == 0)")
     parts = [bitlinear_pack_weights(W, eps, stream=stream)[:2] for W in Ws]
     return torch.cat([p for p, _ in parts]), torch.cat([s for _, s in parts])
 

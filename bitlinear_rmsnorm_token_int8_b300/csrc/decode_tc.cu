@@ -22,10 +22,11 @@
 // (|W . 16 h'| <= 128 K <= 2^21), so the fp32 accumulation is exact.
 //
 // Roles (192 threads):
-//   warp 0      producer: per stage (G segments), one bulk copy per 16-row tile
-//               of its G contiguous 2 KB blocks (tile-major packed layout) and
-//               one bulk copy of the stage's activation blocks (contiguous in
-//               the decode layout), each on its own mbarrier.  The weight
+//   warp 0      producer: per stage (G segments), one bulk copy of the tile's
+//               G segments (contiguous in the tile-major packed layout, up to
+//               32 KB: the copy engine's rate per SM grows with the request
+//               size) and one bulk copy of the stage's activation blocks
+//               (contiguous in the decode layout), each on its own mbarrier.  The weight
 //               copies of the first NS stages are issued before the wait for the
 //               previous kernel, and the decoders start on them at once.
 //   warp 1      allocates 256 TMEM columns (A slots at 0, 64, 128; D at 192),
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
   const int tile = blockIdx.x / S;
   const int s0 = (int)((int64_t)rank * p.nseg / S), s1 = (int)((int64_t)(rank + 1) * p.nseg / S);
   const int nst = (s1 - s0 + p.G - 1) / p.G;                 // stages of this CTA (>= 1)
-  const int nvalid = min(8, p.ntiles16 - tile * 8);          // 16-row tiles that exist
+  const int rows = 16 * min(8, p.ntiles16 - tile * 8);       // weight rows of this tile (<= 128)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
@@ -202,11 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
           if (!lane_wait(empty0 + 8 * slot, (round - 1) & 1, s_abort, p.dev_err)) break;
         }
         const int sg = s0 + st * p.G, gc = min(p.G, s1 - sg);
-        mbar_arrive_expect_tx(full0 + 8 * slot, (uint32_t)(nvalid * gc * 2048));
-        const uint32_t dst = sbase + slot * p.stage_bytes;
-        for (int i = 0; i < nvalid; ++i)
-          bulk_g2s_hint(dst + i * p.G * 2048, p.packed + ((int64_t)(tile * 8 + i) * p.nseg + sg) * 2048,
-                        (uint32_t)(gc * 2048), full0 + 8 * slot, pol);
+        // segments [sg, sg + gc) of the tile: one contiguous range of the packed layout
+        mbar_arrive_expect_tx(full0 + 8 * slot, (uint32_t)(gc * rows * 128));
+        bulk_g2s_hint(sbase + slot * p.stage_bytes,
+                      p.packed + (int64_t)tile * p.nseg * 16384 + (int64_t)sg * rows * 128,
+                      (uint32_t)(gc * rows * 128), full0 + 8 * slot, pol);
         if (waited) issue_x(st);
         else ++deferred;
       }
@@ -261,15 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
   } else {
     // ------------------------------------------------------------ decoders
     const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
-    const bool valid = (r >> 4) < nvalid;
+    const bool valid = r < rows;
     int a = 0;
     bool ok = true;
     for (int st = 0; st < nst && ok && !warp_aborted(s_abort); ++st) {
       const int slot = st % p.NS;
       if (!warp_wait(full0 + 8 * slot, (st / p.NS) & 1, s_abort, p.dev_err)) break;
       const int sg = s0 + st * p.G, gc = min(p.G, s1 - sg);
-      // row r of the stage: row tile r / 16, line r % 16; chunk c stored at c ^ (r % 8)
-      const uint32_t wrow = sbase + slot * p.stage_bytes + (r >> 4) * p.G * 2048 + (r & 15) * 128;
+      // segment g of the stage: rows x 128 bytes; row r at line r, chunk c stored at c ^ (r % 8)
+      const uint32_t wrow = sbase + slot * p.stage_bytes + r * 128;
       for (int g = 0; g < gc && ok; ++g) {
         for (int h = 0; h < 2; ++h) {
           const int as = a % kASlots;
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
               const int c = 4 * h + 2 * cp + cc;
-              const uint4 v = valid ? lds128(wrow + g * 2048 + (uint32_t)((c ^ (r & 7)) << 4))
+              const uint4 v = valid ? lds128(wrow + g * rows * 128 + (uint32_t)((c ^ (r & 7)) << 4))
                                     : make_uint4(0u, 0u, 0u, 0u);
               const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -404,9 +405,11 @@ DecodePlan decode_plan(int64_t M, int64_t N, int64_t K, int sms) {
   pl.Mt = Mt;
   pl.nseg = (int)(act_ops_kpad(K) / 512);
   pl.ntile = (int)((N + kRows - 1) / kRows);
-  pl.G = 1;
-  pl.stage_bytes = pl.G * (kWStageBytes + 4 * 256 * Mt);
   const int64_t fixed = 1024 + red_bytes(Mt) + kBarBytes;
+  const int64_t seg_bytes = kWStageBytes + 4 * 256 * Mt;   // weights + operands of one segment
+  // two segments per stage (32 KB weight copies) when two such stages fit twice per SM
+  pl.G = fixed + 4 * seg_bytes <= kTwoPerSm ? 2 : 1;
+  pl.stage_bytes = (int)(pl.G * seg_bytes);
   int NS = 2;
   while (NS < kMaxStages && fixed + (int64_t)(NS + 1) * pl.stage_bytes <= kTwoPerSm) ++NS;
   pl.NS = NS;

@@ -15,16 +15,21 @@ constexpr int kDevErrTimeout = 7;
 constexpr int kDevErrNonFinite = 9;
 
 // ---- packed weight layout -------------------------------------------------
-// Tile-major and pre-swizzled for the contraction kernels: rows in tiles of 16
-// (N padded to a multiple of 16), K in segments of 512 (padded with zero codes),
-// and per (tile, segment) a contiguous 2048-byte block of 16 rows x 128 bytes in
-// which the 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
-// Byte b of row n's canonical packed row (b = k / 4) lives at
-//   ((n / 16) * nseg + b / 128) * 2048 + (n % 16) * 128 + (((b % 128) / 16) ^ (n % 8)) * 16 + b % 16.
+// Tile-major and pre-swizzled for the contraction kernels: rows padded to
+// Np = N rounded up to 16 and grouped in tiles of 128 (the last tile holds the
+// remaining Np % 128 rows, if any), K in segments of 512 (padded with zero
+// codes), 128 bytes per row and segment.  Tiles follow one another; within a
+// tile of R rows, segment s is one contiguous block of R x 128 bytes, in which
+// the 16-byte chunk c of row r sits at chunk position c ^ (r % 8).  So the
+// weights of any run of segments of one tile are one contiguous range, which
+// one bulk copy moves.  Byte b of row n's canonical packed row (b = k / 4):
+//   (n / 128) * 128 * nseg * 128 + (b / 128) * R * 128 + (n % 128) * 128
+//     + (((b % 128) / 16) ^ (n % 8)) * 16 + b % 16,   R = min(128, Np - 128 (n / 128)).
 constexpr int64_t kSegK = 512;
+constexpr int64_t kTileRows = 128;
 inline int64_t packed_nseg(int64_t K) { return (K + kSegK - 1) / kSegK; }
-inline int64_t packed_tiles(int64_t N) { return (N + 15) / 16; }
-inline int64_t packed_layout_bytes(int64_t N, int64_t K) { return packed_tiles(N) * packed_nseg(K) * 2048; }
+inline int64_t packed_rows(int64_t N) { return (N + 15) / 16 * 16; }
+inline int64_t packed_layout_bytes(int64_t N, int64_t K) { return packed_rows(N) * packed_nseg(K) * 128; }
 
 // ---- pack_weights --------------------------------------------------------
 // Workspace layout (bytes): [0, 2048) 256 uint64 exponent bins of sum|W|,

@@ -119,17 +119,21 @@ __global__ void gamma_finalize_kernel(const unsigned long long* __restrict__ bin
 // One thread per 16-byte chunk of the tiled layout (64 weights of one row; see
 // internal.h): codes of rows >= N or k >= K are 0.
 __global__ void ternarize_pack_kernel(const float* __restrict__ W, int64_t N, int64_t K,
-                                      int64_t nseg, int64_t chunks, const float* __restrict__ gd,
+                                      int64_t nseg, int64_t chunks, int64_t Np, const float* __restrict__ gd,
                                       uint8_t* __restrict__ packed, float* __restrict__ w_scale) {
   const float gamma = gd[0];
   const float d = gd[1];
+  const int64_t full_tiles = Np / 128, tile_chunks = nseg * 128 * 8;   // chunks of a full tile
   for (int64_t ci = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; ci < chunks;
        ci += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t blk = ci >> 7;
-    const int within = (int)(ci & 127);
-    const int r = within >> 3, c = (within & 7) ^ (r & 7);     // logical chunk of this position
-    const int64_t tile = blk / nseg, seg = blk - tile * nseg;
-    const int64_t n = tile * 16 + r;
+    int64_t t = ci / tile_chunks;
+    if (t > full_tiles) t = full_tiles;                          // inside the last, partial tile
+    const int64_t rows = (t < full_tiles) ? 128 : Np - 128 * full_tiles;
+    const int64_t w = ci - t * tile_chunks;                      // chunk index within the tile
+    const int64_t seg = w / (rows * 8);
+    const int q = (int)(w - seg * rows * 8);
+    const int r = q >> 3, c = (q & 7) ^ (r & 7);                 // row in the tile, logical chunk
+    const int64_t n = t * 128 + r;
     const int64_t k0 = seg * 512 + c * 64;
     uint32_t out[4] = {0u, 0u, 0u, 0u};
     if (n < N) {
@@ -178,7 +182,8 @@ cudaError_t launch_pack_weights(const float* W, int64_t N, int64_t K, float eps,
   const int64_t chunks = packed_layout_bytes(N, K) / 16;
   int64_t pblocks = (chunks + 255) / 256;
   if (pblocks > (int64_t)sms * 16) pblocks = (int64_t)sms * 16;
-  ternarize_pack_kernel<<<(unsigned)pblocks, 256, 0, stream>>>(W, N, K, nseg, chunks, gd, packed, w_scale);
+  ternarize_pack_kernel<<<(unsigned)pblocks, 256, 0, stream>>>(W, N, K, nseg, chunks, packed_rows(N), gd, packed,
+                                                               w_scale);
   count_launches(3);
   return cudaGetLastError();
 }

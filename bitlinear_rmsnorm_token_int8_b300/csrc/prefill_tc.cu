@@ -14,8 +14,8 @@
 // Tile: 128 weight rows (MMA M, operand A) x 256 tokens (MMA N, operand B),
 // persistent clusters of CL = 1, 2 or 4 CTAs over tiles (TMA multicast of the
 // activation planes within a cluster, see prefill_tc_kernel).  Roles (320 threads):
-//   warp 0      producer: per 512-k segment, eight 2 KB bulk copies of packed
-//               weights (the tile-major layout); per 128-k step, one bulk copy
+//   warp 0      producer: per 512-k segment, one bulk copy of the tile's packed
+//               weights (up to 16 KB, the tile-major layout); per 128-k step, one bulk copy
 //               per operand plane of the token tile's 32 KB block, already in
 //               the swizzled layout the MMA reads (act_ops.cuh).  Copies are
 //               few and large because the copy engine's cost is per request,
@@ -190,11 +190,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
           const int wslot = ws % kNSW, wround = ws / kNSW;
           if (wround >= 1 && !wait_or_abort(B.empty_w + 8 * wslot, (wround - 1) & 1, &s_abort, p.dev_err))
             break;
-          const int nvalid = max(0, min(8, p.ntiles_n16 - wb * 8));
-          mbar_arrive_expect_tx(B.full_w + 8 * wslot, (uint32_t)(nvalid * 2048));
-          for (int i = 0; i < nvalid; ++i)
-            bulk_g2s(sbase + kOffW + wslot * kWStageBytes + i * 2048,
-                     p.packed + ((int64_t)(wb * 8 + i) * nseg + sg) * 2048, 2048u, B.full_w + 8 * wslot);
+          // the tile's rows of this segment: one contiguous block of the packed layout
+          const int rows = max(0, min(128, 16 * p.ntiles_n16 - wb * 128));
+          mbar_arrive_expect_tx(B.full_w + 8 * wslot, (uint32_t)(rows * 128));
+          if (rows > 0)
+            bulk_g2s(sbase + kOffW + wslot * kWStageBytes,
+                     p.packed + (int64_t)wb * nseg * 16384 + (int64_t)sg * rows * 128, (uint32_t)(rows * 128),
+                     B.full_w + 8 * wslot);
           ++ws;
           if (!waited) {                           // operands come from the previous kernel
             pdl_wait();
@@ -282,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
         if (!warp_wait_or_abort(B.full_w + 8 * wslot, (ws / kNSW) & 1, &s_abort, p.dev_err)) break;
         if (as >= 2 && !warp_wait_or_abort(B.a_empty + 8 * ab, ((as >> 1) - 1) & 1, &s_abort, p.dev_err)) break;
         tc_fence_after();
-        // row r of the stage: row tile r / 16, line r % 16; chunk c stored at c ^ (r % 8)
-        const uint32_t row = sbase + kOffW + wslot * kWStageBytes + (r >> 4) * 2048 + (r & 15) * 128;
+        // row r of the stage: line r; chunk c stored at c ^ (r % 8)
+        const uint32_t row = sbase + kOffW + wslot * kWStageBytes + r * 128;
 #pragma unroll
         for (int cp = 0; cp < 4; ++cp) {        // chunk pairs: 32 TMEM columns each
           uint32_t cols[32];

@@ -1,11 +1,12 @@
 """Host-side index helpers for the packed weight layout (numpy only).
 
 ``bitlinear_pack_weights`` writes the 2-bit codes in the tile-major layout that
-the contraction kernels stream (``include/bitlinear.h``): rows in tiles of 16,
-K in segments of 512 codes (128 bytes per row), and per (tile, segment) one
-contiguous 2048-byte block of 16 rows x 128 bytes, in which the 16-byte chunk
-c of row r sits at chunk position c ^ (r % 8).  Rows past N and codes past K
-are zero.  The canonical form is the row-major [N, K/4] byte matrix of the
+the contraction kernels stream (``include/bitlinear.h``): rows padded to a
+multiple of 16 (Np) and grouped in tiles of 128 (the last tile holds the
+remaining Np % 128 rows, if any), K in segments of 512 codes (128 bytes per
+row); tiles one after another, and within a tile of R rows one contiguous block
+of R x 128 bytes per segment, in which the 16-byte chunk c of row r sits at
+chunk position c ^ (r % 8).  Rows past N and codes past K are zero.  The canonical form is the row-major [N, K/4] byte matrix of the
 code table (weight k of row n in byte k/4, bits 2(k%4)..2(k%4)+1).
 
 These functions only move bytes; they hold none of the method's arithmetic.
@@ -15,21 +16,25 @@ from __future__ import annotations
 import numpy as np
 
 SEG_K = 512
-TILE_N = 16
-BLOCK_BYTES = 2048
+ROW_PAD = 16
+TILE_N = 128
+ROW_BYTES = 128          # one row of one segment
 
 
 def packed_bytes(N: int, K: int) -> int:
     """Size of the tiled layout for an N x K weight matrix."""
-    return -(-N // TILE_N) * -(-K // SEG_K) * BLOCK_BYTES
+    return -(-N // ROW_PAD) * ROW_PAD * -(-K // SEG_K) * ROW_BYTES
 
 
 def packed_index(N: int, K: int) -> np.ndarray:
     """int64 [N, K/4]: offset in the tiled layout of each canonical packed byte."""
     nseg = -(-K // SEG_K)
+    Np = -(-N // ROW_PAD) * ROW_PAD
     n = np.arange(N, dtype=np.int64)[:, None]
     b = np.arange(K // 4, dtype=np.int64)[None, :]
-    return (((n // TILE_N) * nseg + b // 128) * BLOCK_BYTES + (n % TILE_N) * 128
+    t = n // TILE_N
+    rows = np.minimum(TILE_N, Np - t * TILE_N)           # rows of this tile
+    return (t * TILE_N * nseg * ROW_BYTES + (b // 128) * rows * ROW_BYTES + (n % TILE_N) * ROW_BYTES
             + (((b % 128) // 16) ^ (n % 8)) * 16 + b % 16)
 
 

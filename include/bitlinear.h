@@ -105,8 +105,19 @@ size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K);
  * W        [N,K] fp32, nn.Linear layout (row n = output feature n).  Must be finite.
  * N, K     N >= 1, K >= 4, K % 4 == 0, N*K < 2^32.
  * eps      the eps of the divisor (1e-5 in BitNet b1.58); must be >= 0.
- * packed   [N, K/4] uint8 out: weight k of row n in byte n*K/4 + k/4, bits
- *          2*(k%4)..2*(k%4)+1, code 00 = 0, 01 = +1, 10 = -1 (11 never written).
+ * packed   bitlinear_packed_bytes(N,K) uint8 out.  The codes of one row form the
+ *          canonical packed row: weight k in byte k/4, bits 2*(k%4)..2*(k%4)+1,
+ *          code 00 = 0, 01 = +1, 10 = -1 (11 never written).  The rows are stored
+ *          tile-major for the contraction kernels: rows padded to Np = N rounded
+ *          up to 16 and grouped in tiles of 128 (the last tile holds the remaining
+ *          Np % 128), K padded to Kp = K rounded up to 512 (segments of 128 bytes
+ *          per row); within a tile of R rows each segment is one contiguous block
+ *          of R x 128 bytes, and byte b of row n's canonical row sits at
+ *            (n/128)*128*(Kp/512)*128 + (b/128)*R*128 + (n%128)*128
+ *              + (((b%128)/16) ^ (n%8))*16 + b%16.
+ *          Padding holds zero codes.  Concatenating the outputs for matrices of
+ *          N_i rows gives the packing of the stacked matrix when every N_i but the
+ *          last is a multiple of 128.
  * w_scale  [N] fp32 out: gamma repeated for every row (a per-row scale vector lets
  *          several matrices be stacked into one fused projection).
  * gamma_out [1] fp32 out, or NULL.

@@ -180,9 +180,13 @@ def test_packed_layout_swizzle_example():
     # chunk 1 ^ 1 = 0 -> offset 9*128 + 0*16 + 4
     from bitlinear_rmsnorm_token_int8_b300 import layout
     assert layout.packed_index(16, 512)[9, 20] == 9 * 128 + 4
-    # row 16 starts tile 1 after all segments of tile 0: K = 1024 -> 2 segments
-    assert layout.packed_index(17, 1024)[16, 0] == 2 * 2048
-    assert layout.packed_index(17, 1024)[0, 128] == 2048      # segment 1 of tile 0
+    # segment 1 of a full tile starts after the 128 rows of segment 0
+    assert layout.packed_index(130, 1024)[0, 128] == 128 * 128
+    # row 128 starts tile 1 after both segments of tile 0 (K = 1024 -> 2 segments)
+    assert layout.packed_index(130, 1024)[128, 0] == 2 * 128 * 128
+    # the last tile holds the 16 rows of N = 130 padded to 144: its segment blocks are 16 x 128 bytes
+    assert layout.packed_index(130, 1024)[129, 128] == 2 * 128 * 128 + 16 * 128 + 1 * 128 + (0 ^ 1) * 16
+    assert layout.packed_bytes(130, 1024) == 144 * 2 * 128
 
 
 def _lib_bytes(N, K):
