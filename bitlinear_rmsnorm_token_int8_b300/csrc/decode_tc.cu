@@ -173,6 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
   const uint32_t tmem = *s_tmem;
 
   int acc[Mt];                               // epilogue warps: this row's sums per token
+  float as_reg[Mt];                          // per-token scales
+  float res_reg[Mt];                         // residual inputs (out_dtype 2)
+  float wsn_reg = 0.0f;                      // this row's weight scale
   bool have = false;
   const int r = 32 * (warp & 3) + lane;      // decoder / epilogue row within the tile
 
@@ -313,6 +316,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
 
     // ------------------------------------------------------------ epilogue
     pdl_wait();                              // act_scale and y follow the stream order
+    // The scales are loaded now, while the MMAs finish: in the store loop below
+    // the compiler could not move them above the (possibly aliasing) y stores.
+#pragma unroll
+    for (int m = 0; m < Mt; ++m) as_reg[m] = m < p.M ? __ldcg(p.act_scale + m) : 0.0f;
+    wsn_reg = (tile * kRows + r < p.N) ? __ldg(p.w_scale + tile * kRows + r) : 0.0f;
+    if (p.out_dtype == 2 && rank == 0 && tile * kRows + r < p.N) {   // the residuals, for the same reason
+      const unsigned short* yr = reinterpret_cast<const unsigned short*>(p.y) + tile * kRows + r;
+#pragma unroll
+      for (int m = 0; m < Mt; ++m)
+        res_reg[m] = m < p.M ? __uint_as_float((uint32_t)__ldcg(yr + (size_t)m * p.N) << 16) : 0.0f;
+    }
     if (!warp_aborted(s_abort) && warp_wait(dfull, 0, s_abort, p.dev_err)) {
       tc_fence_after();
       uint32_t d[Nmma];
@@ -346,12 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
   if (warp >= 2 && have && rank == 0) {
     const int n = tile * kRows + r;
     if (n < p.N && !*s_abort) {
-      const float wsn = __ldg(p.w_scale + n);
+      const float wsn = wsn_reg;
 #pragma unroll
       for (int m = 0; m < Mt; ++m) {
         if (m < p.M) {
           const int v = S > 1 ? acc[m] + s_red[m * kRows + r] : acc[m];
-          const float as = __ldcg(p.act_scale + m);
+          const float as = as_reg[m];
           const size_t o = (size_t)m * p.N + n;
           const float yv = __fmul_rn(__fmul_rn((float)v, as), wsn);
           if (p.out_dtype == 0) {
@@ -359,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
           } else {
             __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o;
             // out_dtype 2: residual add into the bf16 output, y = bf16(y + result)
-            *yb = __float2bfloat16_rn(p.out_dtype == 2 ? __fadd_rn(__bfloat162float(*yb), yv) : yv);
+            *yb = __float2bfloat16_rn(p.out_dtype == 2 ? __fadd_rn(res_reg[m], yv) : yv);
           }
           if (p.acc_debug) p.acc_debug[o] = v;
         }

@@ -364,12 +364,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
           }
         } else {                                             // bf16 residual add
           __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o0;
+          // residuals 16 at a time, loaded before the stores: a load after a store to y
+          // could not be moved ahead of it
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float as = __shfl_sync(0xffffffffu, as_lane[c], j);
-            if (j < jmax) {
-              const float yv = __fmul_rn(__fmul_rn(__uint_as_float(rv[c & 1][j]), as), wsn);
-              yb[(size_t)j * p.N] = __float2bfloat16_rn(__fadd_rn(__bfloat162float(yb[(size_t)j * p.N]), yv));
+          for (int hh = 0; hh < 2; ++hh) {
+            float res[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = 16 * hh + jj;
+              res[jj] = j < jmax ? __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(yb) +
+                                                                     (size_t)j * p.N) << 16)
+                                 : 0.0f;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = 16 * hh + jj;
+              const float as = __shfl_sync(0xffffffffu, as_lane[c], j);
+              if (j < jmax) {
+                const float yv = __fmul_rn(__fmul_rn(__uint_as_float(rv[c & 1][j]), as), wsn);
+                yb[(size_t)j * p.N] = __float2bfloat16_rn(__fadd_rn(res[jj], yv));
+              }
             }
           }
         }
