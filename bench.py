@@ -256,7 +256,8 @@ def traffic_record(kernel_src: str):
 
 def measure_prefill(bl, synth, torch, dev, steps, warmup):
     """M = 2048 prefill of the 8B-class shapes (4096->14336, 14336->4096): per shape one
-    graph of RMSNorm + quantization + contraction; CUDA events around `steps` replays.
+    graph of the whole BitLinear layer (bitlinear_linear_forward: RMSNorm + quantization
+    into the operand form, then the contraction); CUDA events around `steps` replays.
     Reports int8-equivalent TOPS (2 M N K / time) of the quant + contraction pair and
     of the contraction alone, and the contraction's tensor-core rate against the
     measured peak: it issues two e4m3 MMAs per int8 product, i.e. 4 M N K fp8 FLOP."""
@@ -271,19 +272,22 @@ def measure_prefill(bl, synth, torch, dev, steps, warmup):
         del W
         x = synth.activations(M, p.K, synth.act_seed(wl.seed, M, p.K), outliers=True).to(dev)
         g = synth.rms_gains(p.K, synth.gain_seed(wl.seed, 0, pi)).to(dev)
-        xq = torch.empty((M, p.K), dtype=torch.int8, device=dev)
         sc = torch.empty(M + 4, dtype=torch.float32, device=dev)[:M]
         ops = torch.empty(bl.bitlinear_act_ops_bytes(M, p.K), dtype=torch.uint8, device=dev)
+        ws = torch.empty(bl.bitlinear_linear_workspace_bytes(M, p.N, p.K), dtype=torch.uint8, device=dev)
         y = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+        # operands and scales for the contraction-only graph
+        bl.bitlinear_quant_act(x, g, RMS_EPS, act_scale=sc, x_ops=ops)
         graphs = {}
         with torch.cuda.stream(stream):
             for kind in ("pair", "fwd"):
                 def run(kind=kind):
                     if kind == "pair":
-                        bl.bitlinear_quant_act(x, g, RMS_EPS, x_q=xq, act_scale=sc, x_ops=ops, flags=bl.FLAG_PDL,
-                                               stream=stream)
-                    bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=torch.bfloat16, y=y, x_ops=ops,
-                                         flags=bl.FLAG_PDL, K=p.K, stream=stream)
+                        bl.bitlinear_linear_forward(x, g, RMS_EPS, packed, w_scale, out_dtype=torch.bfloat16, y=y,
+                                                    workspace=ws, flags=bl.FLAG_PDL, stream=stream)
+                    else:
+                        bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=torch.bfloat16, y=y, x_ops=ops,
+                                             flags=bl.FLAG_PDL, K=p.K, stream=stream)
                 run()
                 stream.synchronize()
                 gr = torch.cuda.CUDAGraph()
@@ -308,7 +312,7 @@ def measure_prefill(bl, synth, torch, dev, steps, warmup):
         tot_ops += ops_
         tot_ms += ms["pair"]
         tot_fwd_ms += ms["fwd"]
-        del packed, w_scale, x, xq, ops, y, graphs
+        del packed, w_scale, x, ops, ws, y, graphs
     _, bf16_tf, src = measured_peaks()
     fp8_peak = 2.0 * bf16_tf          # e4m3 dense rate = 2x bf16 (nominal ratio)
     fwd_tflops = 2.0 * tot_ops / (tot_fwd_ms * 1e9)

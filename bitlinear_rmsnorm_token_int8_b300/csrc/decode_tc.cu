@@ -385,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
 // x_q -> activation operands, for callers that did not get them from quant_act.
 __global__ void act_ops_from_codes_kernel(const int8_t* __restrict__ x_q, int64_t M, int64_t K,
                                           int64_t Kp, uint8_t* __restrict__ ops) {
+  pdl_launch_dependents();                   // the next kernel waits for this one to complete
   pdl_wait();
-  pdl_launch_dependents();
   const int64_t per_row = Kp >> 4;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < M * per_row;
        idx += (int64_t)gridDim.x * blockDim.x) {

@@ -135,8 +135,11 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
         gv_[i][hv] = (gain && tid + i * T < U && v < V) ? __ldg(gain + v) : kOnes;
       }
   }
-  pdl_wait();                                // x may be the previous kernel's output
+  // Let the next kernel launch now: it waits for this one to complete, and this one
+  // completes only after the kernel before it (the wait below), so the next kernel
+  // can set up and prefetch its weights while the previous one still runs.
   pdl_launch_dependents();
+  pdl_wait();                                // x may be the previous kernel's output
   const uint4* xr = x + (size_t)row * ld;
   const float* gr = glu ? glu + (size_t)row * 2 * K : nullptr;
 
@@ -245,6 +248,166 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
   }
 }
 
+// Many rows (prefill): persistent CTAs, kRowsThreads threads each, take rows
+// blockIdx.x, blockIdx.x + gridDim.x, ...  A row is staged in shared memory by
+// one bulk copy into a double buffer, so the copy of the next row overlaps the
+// work on this one; the gain is staged once.  Same arithmetic as
+// quant_act_kernel, in two passes over the staged row.
+constexpr int kRowsThreads = 256;
+constexpr uint32_t kRowsSpin = 1u << 24;
+
+__global__ void __launch_bounds__(kRowsThreads, 2)
+quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __restrict__ gain, float rms_eps,
+                  int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale, uint8_t* __restrict__ x_ops,
+                  int64_t M, int* dev_err) {
+  extern __shared__ __align__(16) uint8_t qsm[];
+  const int rb = K * 2;                            // bytes of a row (a multiple of 16)
+  const uint32_t buf0 = smem_u32(qsm), gbuf = buf0 + 2 * rb;
+  __shared__ uint64_t bars[2];
+  __shared__ float s_max[kRowsThreads / 32];
+  __shared__ float2 s_ss[kRowsThreads / 32];
+  __shared__ float s_m, s_sum;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = K >> 3, U = (V + 1) >> 1;
+  const int64_t Kp = act_ops_kpad(K);
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  // the gain is not written by earlier kernels: stage it before waiting for them
+  for (int v = tid; v < V; v += kRowsThreads)
+    *reinterpret_cast<uint4*>(qsm + 2 * rb + 16 * v) =
+        gain ? __ldg(reinterpret_cast<const uint4*>(gain) + v) : kOnes;
+  __syncthreads();
+  pdl_launch_dependents();                         // as in quant_act_kernel
+  pdl_wait();                                      // x may be the previous kernel's output
+  // thread 0 issues the copies; `pend` = iteration whose copy is issued and not yet waited for
+  int pend = -1;
+  auto issue = [&](int64_t row, int iter) {
+    const int b = iter & 1;
+    mbar_arrive_expect_tx(smem_u32(&bars[b]), (uint32_t)rb);
+    bulk_g2s(buf0 + b * rb, x + row * ld, (uint32_t)rb, smem_u32(&bars[b]));
+  };
+  if (tid == 0 && (int64_t)blockIdx.x < M) {
+    issue(blockIdx.x, 0);
+    pend = 0;
+  }
+  int it = 0;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x, ++it) {
+    const int b = it & 1;
+    if (tid == 0) {
+      if (!mbar_wait_bounded(smem_u32(&bars[b]), (uint32_t)((it >> 1) & 1), kRowsSpin)) {
+        atomicCAS(dev_err, 0, kDevErrTimeout);
+        s_abort = 1;
+      } else {
+        pend = -1;
+        if (row + gridDim.x < M) {                // the other buffer was released at the end of the last row
+          issue(row + gridDim.x, it + 1);
+          pend = it + 1;
+        }
+      }
+    }
+    __syncthreads();
+    if (s_abort) break;
+    if (!mbar_wait_bounded(smem_u32(&bars[b]), (uint32_t)((it >> 1) & 1), kRowsSpin)) break;  // complete: acquires the data
+    const uint32_t xb = buf0 + b * rb;
+    // pass 1: max |x g| (exact) and sum x^2 as an error-free pair
+    float amax = 0.0f, hi = 0.0f, lo = 0.0f;
+    for (int u = tid; u < U; u += kRowsThreads) {
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        const int v = 2 * u + hv;
+        if (v < V) {
+          float xf[8], gf[8];
+          unpack8(lds128(xb + 16 * v), xf);
+          unpack8(lds128(gbuf + 16 * v), gf);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            amax = fmaxf(amax, fabsf(__fmul_rn(xf[j], gf[j])));
+            float s_, e_;
+            two_sum(hi, __fmul_rn(xf[j], xf[j]), s_, e_);
+            hi = s_;
+            lo = __fadd_rn(lo, e_);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+      pair_add(hi, lo, h2, l2);
+    }
+    if (lane == 0) {
+      s_max[warp] = amax;
+      s_ss[warp] = make_float2(hi, lo);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float a = lane < kRowsThreads / 32 ? s_max[lane] : 0.0f;
+      float2 p2 = lane < kRowsThreads / 32 ? s_ss[lane] : make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        const float h2 = __shfl_xor_sync(0xffffffffu, p2.x, o), l2 = __shfl_xor_sync(0xffffffffu, p2.y, o);
+        pair_add(p2.x, p2.y, h2, l2);
+      }
+      if (lane == 0) {
+        s_m = a;
+        s_sum = __fadd_rn(p2.x, p2.y);
+      }
+    }
+    __syncthreads();
+    const float m = fmaxf(s_m, 1e-8f);
+    const float sc = __fdiv_rn(127.0f, m);
+    if (tid == 0) {
+      float sigma = __fdiv_rn(m, 127.0f);
+      if (rms_eps >= 0.0f) {
+        const float ms = __fdiv_rn(s_sum, (float)K);
+        const float r = __frsqrt_rn(__fadd_rn(ms, rms_eps));
+        sigma = __fdiv_rn(__fmul_rn(m, r), 127.0f);
+      }
+      act_scale[row] = sigma;
+    }
+    // pass 2: codes, the int8 row and the operand form
+    uint2* qr = x_q ? reinterpret_cast<uint2*>(x_q + row * K) : nullptr;
+    for (int u = tid; u < (int)(Kp >> 4); u += kRowsThreads) {
+      int q[16];
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        const int v = 2 * u + hv;
+        if (v < V) {
+          float xf[8], gf[8];
+          unpack8(lds128(xb + 16 * v), xf);
+          unpack8(lds128(gbuf + 16 * v), gf);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) q[8 * hv + j] = quant_code(__fmul_rn(xf[j], gf[j]), sc, m);
+          if (qr) {
+            uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              w0 |= (uint32_t)(q[8 * hv + j] & 0xff) << (8 * j);
+              w1 |= (uint32_t)(q[8 * hv + j + 4] & 0xff) << (8 * j);
+            }
+            qr[v] = make_uint2(w0, w1);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) q[8 * hv + j] = 0;     // padding up to Kp: zero operands
+        }
+      }
+      if (x_ops) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, q);
+    }
+    __syncthreads();                               // buffer b is free for the row after next
+  }
+  // no copy may still be landing in shared memory when the CTA exits
+  if (tid == 0 && pend >= 0 && !mbar_wait_bounded(smem_u32(&bars[pend & 1]), (uint32_t)((pend >> 1) & 1), kRowsSpin))
+    atomicCAS(dev_err, 0, kDevErrTimeout);
+}
+
 }  // namespace
 
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,
@@ -257,6 +420,36 @@ cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu,
                                 float rms_eps, int64_t M, int64_t K, int8_t* x_q, float* act_scale,
                                 uint8_t* x_ops, bool pdl, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
+  const int sms = num_sms();
+  // Many long rows of bf16 input: persistent CTAs that stream rows through shared
+  // memory.  Measured: faster from K > 4096 with at least four rows per SM; shorter
+  // rows or fewer of them stay with one CTA per row.
+  const int64_t rows_smem = 6 * K;            // two row buffers + the gain
+  if (!glu && M >= 4 * sms && K > 4096 && rows_smem <= 100 * 1024) {
+    int* dev_err = current_device_error_word();
+    if (!dev_err) return cudaErrorInvalidDevice;
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(quant_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           100 * 1024);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(M < 2 * sms ? M : 2 * sms), 1, 1);
+    cfg.blockDim = dim3(kRowsThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)rows_smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, quant_rows_kernel, x, ld, gain, rms_eps, (int)K, x_q, act_scale,
+                                       x_ops, M, dev_err);
+    count_launches(1);
+    return e;
+  }
   const int U = (int)((K / 8 + 1) / 2);       // units of 16 inputs
   int T, vpt;
   // Few rows (decode): each row is one CTA's serial chain, so spread it over up
@@ -264,7 +457,7 @@ cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu,
   if (U <= 256) {
     T = ((U + 31) / 32) * 32;
     vpt = 1;
-  } else if (M < num_sms() || U > 1024) {
+  } else if (M < sms || U > 1024) {
     T = U <= 1024 ? ((U + 31) / 32) * 32 : 1024;
     vpt = (U + T - 1) / T;
   } else {

@@ -87,6 +87,19 @@ def test_quant_act_matches_oracle(M, K, gain, rms, outliers):
     assert np.all(np.abs(sc - osig) <= SIGMA_RTOL * osig)
 
 
+@pytest.mark.parametrize("M,K,gain,rms", [(600, 4104, True, True), (640, 6912, False, True), (700, 8192, True, False)])
+def test_quant_act_many_rows_matches_oracle(M, K, gain, rms):
+    # M >= 4 x the SM count and K > 4096: persistent CTAs streaming rows through
+    # shared memory; K = 4104 ends in half a 16-input unit
+    x = synth.activations(M, K, seed=M + 3 * K)
+    g = synth.rms_gains(K, seed=K + 1) if gain else None
+    eps = RMS_EPS if rms else -1.0
+    xq, sc = gpu_quant(x, g, eps)
+    oq, osig = oracle.act_quant(synth.bf16_bits(x), None if g is None else synth.bf16_bits(g), eps)
+    assert (xq == oq).all()
+    assert np.all(np.abs(sc - osig) <= SIGMA_RTOL * osig)
+
+
 def test_quant_act_edge_rows():
     K = 512
     rows = np.zeros((6, K), dtype=np.float32)
