@@ -61,6 +61,23 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def max_over_ranks(value: float, pg, device) -> float:
+    """The largest `value` over all ranks (the slowest replica sets the step time);
+    `pg` is torch.distributed (or None for one process)."""
+    if pg is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(world: int, bytes_per_step_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job GB/s of N replicas that each stream `bytes_per_step_per_rank` per step,
+    timed by the slowest one."""
+    return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -423,12 +440,8 @@ def our_arm(args):
         torch.cuda.synchronize()
     barrier()
     launches = launches_per_step * args.steps
-    ms = start.elapsed_time(end) / args.steps
-    if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * packed_bytes_step / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps, pg, dev)
+    value = aggregate_gbs(world, packed_bytes_step, ms)
 
     # ---- per-launch durations of the contraction kernel.  For each (M, projection) a
     #      CUDA graph holds the 30 layers' forward launches back to back (distinct weights,
@@ -470,30 +483,44 @@ def our_arm(args):
             alg_bytes_fwd.append(p.N * p.K // 4 + 2 * M * p.K + 4 * M + 4 * p.N + 2 * M * p.N)
     per_step_launches = len(alg_bytes_fwd)
 
-    # ---- end to end through the public API: pinned host inputs in, bf16 outputs out
-    host_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
-    host_y = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in ys.items()}
-    dev_x = {k: torch.empty_like(v) for k, v in xs.items()}
+    # ---- end to end through the public API: pinned host inputs in, bf16 outputs out.
+    #      Every projection of the step gets its own input rows; they travel to the
+    #      device as one copy from one pinned buffer, and all outputs come back as one
+    #      copy, the way a caller stages a step's data.
+    in_off, out_off = {}, {}
     h2d = d2h = 0
     for M in wl.tokens:
-        for row in weights:
-            for (p, _, _) in row:
+        for li, row in enumerate(weights):
+            for pi, (p, _, _) in enumerate(row):
+                in_off[(M, li, pi)] = h2d // 2
+                out_off[(M, li, pi)] = d2h // 2
                 h2d += M * p.K * 2
                 d2h += M * p.N * 2
+    host_in = torch.empty(h2d // 2, dtype=torch.bfloat16, pin_memory=True)
+    host_out = torch.empty(d2h // 2, dtype=torch.bfloat16, pin_memory=True)
+    for M in wl.tokens:
+        for li, row in enumerate(weights):
+            for pi, (p, _, _) in enumerate(row):
+                o = in_off[(M, li, pi)]
+                host_in[o:o + M * p.K].copy_(xs[(M, p.K)].reshape(-1).cpu())
+    dev_in = torch.empty_like(host_in, device=dev)
+    dev_out = torch.empty_like(host_out, device=dev)
 
     def e2e_step():
-        """Per projection: pinned host x -> device, RMSNorm + quant, contraction, y -> pinned host."""
+        """Inputs in (one copy), per projection RMSNorm + quant and the contraction, outputs out (one copy)."""
+        dev_in.copy_(host_in, non_blocking=True)
         for M in wl.tokens:
-            for row in weights:
-                for (p, packed, w_scale) in row:
-                    dev_x[(M, p.K)].copy_(host_x[(M, p.K)], non_blocking=True)
-                    bl.bitlinear_quant_act(dev_x[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)],
-                                           act_scale=sc[(M, p.K)], x_ops=ops[(M, p.K)], flags=FL,
-                                           stream=stream)
-                    y = bl.bitlinear_forward(None, sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
-                                             y=ys[(M, p.N)], x_ops=ops[(M, p.K)], flags=FL, K=p.K,
-                                             stream=stream)
-                    host_y[(M, p.N)].copy_(y, non_blocking=True)
+            for li, row in enumerate(weights):
+                for pi, (p, packed, w_scale) in enumerate(row):
+                    o = in_off[(M, li, pi)]
+                    x = dev_in[o:o + M * p.K].view(M, p.K)
+                    yo = out_off[(M, li, pi)]
+                    y = dev_out[yo:yo + M * p.N].view(M, p.N)
+                    bl.bitlinear_quant_act(x, gains[p.K], RMS_EPS, x_q=xq[(M, p.K)], act_scale=sc[(M, p.K)],
+                                           x_ops=ops[(M, p.K)], flags=FL, stream=stream)
+                    bl.bitlinear_forward(None, sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16, y=y,
+                                         x_ops=ops[(M, p.K)], flags=FL, K=p.K, stream=stream)
+        host_out.copy_(dev_out, non_blocking=True)
 
     # the e2e step as one graph too: copy nodes from/to pinned host memory around the
     # library calls, so the number is not Python launch overhead
@@ -513,12 +540,8 @@ def our_arm(args):
             e2e_graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * packed_bytes_step / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, dev)
+    e2e_value = aggregate_gbs(world, packed_bytes_step, e2e_ms)
 
     # ---- roofline of the dominant kernel (the contraction)
     hbm, bf16_tf, peak_src = measured_peaks()
