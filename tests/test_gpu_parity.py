@@ -291,6 +291,8 @@ def test_forward_from_quant_operands_matches_oracle(M, N, K, dt, pdl):
     (300, 384, 2560, torch.float32),    # ragged second token tile
     (512, 256, 384, torch.bfloat16),    # K % 512 == 384: a zero-padded segment tail
     (80, 128, 14336, torch.float32),    # long K: |acc| up to 127 * 14336
+    (256, 19200, 512, torch.bfloat16),  # 75 tiles on 74 clusters: the last one split in 16 x 16 tokens
+    (300, 13824, 512, torch.float32),   # 108 tiles: the last wave in sub-tiles of 128 tokens
 ])
 def test_prefill_matches_oracle(M, N, K, dt):
     # M > 32 tokens run on the tcgen05 kernel (weights decoded into tensor memory)
