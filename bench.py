@@ -506,10 +506,32 @@ def our_arm(args):
     dev_in = torch.empty_like(host_in, device=dev)
     dev_out = torch.empty_like(host_out, device=dev)
 
+    side = torch.cuda.Stream(device=dev)       # host<->device copies, beside the kernels
+    in_rng = {}                                 # element range of each pass's inputs
+    for M in wl.tokens:
+        lo = in_off[(M, 0, 0)]
+        last = (M, len(weights) - 1, len(wl.projections) - 1)
+        in_rng[M] = (lo, in_off[last] + M * wl.projections[-1].K)
+    out_rng = {}                                # element range of each (pass, layer)'s outputs
+    for M in wl.tokens:
+        for li in range(len(weights)):
+            lo = out_off[(M, li, 0)]
+            out_rng[(M, li)] = (lo, out_off[(M, li, len(wl.projections) - 1)] + M * wl.projections[-1].N)
+
     def e2e_step():
-        """Inputs in (one copy), per projection RMSNorm + quant and the contraction, outputs out (one copy)."""
-        dev_in.copy_(host_in, non_blocking=True)
+        """Inputs in, per projection RMSNorm + quant and the contraction, outputs out.  The
+        copies run on a side stream: each pass's inputs as one copy (the second pass's
+        while the first computes), each layer's outputs as soon as the layer is done."""
+        side.wait_stream(stream)
+        ev_in = {}
+        with torch.cuda.stream(side):
+            for M in wl.tokens:
+                lo, hi = in_rng[M]
+                dev_in[lo:hi].copy_(host_in[lo:hi], non_blocking=True)
+                ev_in[M] = torch.cuda.Event()
+                ev_in[M].record(side)
         for M in wl.tokens:
+            stream.wait_event(ev_in[M])
             for li, row in enumerate(weights):
                 for pi, (p, packed, w_scale) in enumerate(row):
                     o = in_off[(M, li, pi)]
@@ -520,7 +542,13 @@ def our_arm(args):
                                            x_ops=ops[(M, p.K)], flags=FL, stream=stream)
                     bl.bitlinear_forward(None, sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16, y=y,
                                          x_ops=ops[(M, p.K)], flags=FL, K=p.K, stream=stream)
-        host_out.copy_(dev_out, non_blocking=True)
+                done = torch.cuda.Event()
+                done.record(stream)
+                side.wait_event(done)
+                with torch.cuda.stream(side):
+                    lo, hi = out_rng[(M, li)]
+                    host_out[lo:hi].copy_(dev_out[lo:hi], non_blocking=True)
+        stream.wait_stream(side)
 
     # the e2e step as one graph too: copy nodes from/to pinned host memory around the
     # library calls, so the number is not Python launch overhead
