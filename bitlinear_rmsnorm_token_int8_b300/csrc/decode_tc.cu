@@ -19,16 +19,16 @@
 // decode layout): columns [0, Mt) accumulate W . (16 h'), [Mt, 2 Mt) W . l', so
 // one m128 x n(2 Mt) x k32 MMA covers both, and the exact integer sum of a row
 // and token is D[m] + D[Mt + m].  Each column stays below 2^24 in magnitude
-// (|W . 16 h'| <= 128 K <= 2^21), so the fp32 accumulation is exact.
+// (|W . 16 h'| <= 128 K <= 2^23 for K <= 65536), so the fp32 accumulation is exact.
 //
 // Roles (192 threads):
 //   warp 0      producer: per stage (G segments), one bulk copy of the tile's
 //               G segments (contiguous in the tile-major packed layout, up to
 //               32 KB: the copy engine's rate per SM grows with the request
 //               size) and one bulk copy of the stage's activation blocks
-//               (contiguous in the decode layout), each on its own mbarrier.  The weight
-//               copies of the first NS stages are issued before the wait for the
-//               previous kernel, and the decoders start on them at once.
+//               (contiguous in the decode layout), each on its own mbarrier.
+//               The weight copies of the first NS stages are issued before the
+//               wait for the previous kernel, and the decoders start on them.
 //   warp 1      allocates 256 TMEM columns (A slots at 0, 64, 128; D at 192),
 //               one lane issues 8 MMAs per half segment (256 k) and commits.
 //   warps 2-5   decoders, thread = weight row: 2-bit codes -> e4m3 bytes by
@@ -69,7 +69,7 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxSplit = 8;                // portable cluster size
 constexpr uint32_t kSpin = 1u << 24;
 constexpr uint32_t kCodeToE4M3 = 0x00B83800u;  // bytes 0x00 (code 0), 0x38 (+1), 0xB8 (-1)
-constexpr int kWStageBytes = 8 * 2048;      // per segment: 8 row tiles x one 2 KB block
+constexpr int kWStageBytes = 128 * 128;     // per segment: 128 rows x 128 bytes of packed codes
 constexpr int64_t kTwoPerSm = 115712;       // 2 x (this + 1 KB reserved) = 228 KB per SM
 constexpr int64_t kThreePerSm = 76800;      // above this, a third CTA does not fit
 

@@ -13,13 +13,13 @@
 //
 // Tile: 128 weight rows (MMA M, operand A) x 256 tokens (MMA N, operand B),
 // persistent clusters of CL = 1, 2 or 4 CTAs over tiles (TMA multicast of the
-// activation planes within a cluster, see prefill_tc_kernel).  Roles (320 threads):
+// activation planes within a cluster, see prefill_tc_kernel).  Roles (448 threads):
 //   warp 0      producer: per 512-k segment, one bulk copy of the tile's packed
-//               weights (up to 16 KB, the tile-major layout); per 128-k step, one bulk copy
-//               per operand plane of the token tile's 32 KB block, already in
-//               the swizzled layout the MMA reads (act_ops.cuh).  Copies are
-//               few and large because the copy engine's cost is per request,
-//               and per 128-byte row for tensor-map boxes.
+//               weights (up to 16 KB, the tile-major layout); per 128-k step,
+//               one bulk copy per operand plane of the token tile's 32 KB block,
+//               already in the swizzled layout the MMA reads (act_ops.cuh).
+//               Copies are few and large because the copy engine's cost is per
+//               request, and per 128-byte row for tensor-map boxes.
 //   warp 1      allocates TMEM (512 columns: D = 256, A = 2 x 128); one lane
 //               issues the MMAs: per 128-k step, 4 k32 steps x 2 planes.
 //   warps 2-5   decoders: thread = weight row; 2-bit codes -> e4m3 bytes by
@@ -61,7 +61,7 @@ constexpr int kNSX = 3;                     // operand stages (128 k each)
 constexpr int kNSW = 2;                     // weight stages (512 k each)
 constexpr int kXPlaneBytes = kTileT * 128;  // 32 KB
 constexpr int kXStageBytes = 2 * kXPlaneBytes;
-constexpr int kWStageBytes = 8 * 2048;      // 8 row tiles x one 2 KB block
+constexpr int kWStageBytes = 128 * 128;     // one segment: 128 rows x 128 bytes of packed codes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 256;             // A buffers at columns 256 and 384
 constexpr uint32_t kSpin = 1u << 24;
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       for (int ct = cid; ct < ctiles && !s_abort; ct += ncl) {
         const int wb = (ct % nwbg) * CL + rank, tt = ct / nwbg;
         for (int sg = 0; sg < nseg && !s_abort; ++sg) {
-          // weights of this segment: the eight 16-row tiles of the block
+          // weights of this segment
           const int wslot = ws % kNSW, wround = ws / kNSW;
           if (wround >= 1 && !wait_or_abort(B.empty_w + 8 * wslot, (wround - 1) & 1, &s_abort, p.dev_err))
             break;
