@@ -90,6 +90,9 @@ int num_sms();
 
 // ---- tensor maps and the prefill contraction ---------------------------------
 
+// Tokens per tile of the prefill contraction (256, or 128 when that fills more SMs).
+int prefill_tile_tokens(int64_t M, int64_t N, int sms);
+
 cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
                               const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
                               void* y, int32_t* acc_debug, int* dev_err, bool pdl,

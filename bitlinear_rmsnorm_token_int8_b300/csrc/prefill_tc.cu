@@ -11,16 +11,20 @@
 // two MMAs per k step into one fp32 accumulator, exact while |acc| < 2^24
 // (|acc| <= 127 K <= 2^23).
 //
-// Tile: 128 weight rows (MMA M, operand A) x 256 tokens (MMA N, operand B),
-// persistent clusters of CL = 1, 2 or 4 CTAs over tiles (TMA multicast of the
-// activation planes within a cluster, see prefill_tc_kernel).  Roles (448 threads):
+// Tile: 128 weight rows (MMA M, operand A) x TT = 256 or 128 tokens (MMA N,
+// operand B), persistent clusters of CL = 1 or 2 CTAs over tiles (TMA multicast
+// of the activation planes within a cluster, see prefill_tc_kernel).
+// 128-token tiles double the number of tiles where 256-token ones would leave
+// many SMs idle (a few hundred tokens, or a last wave at most half full); the
+// operand layout is the same (a 128-token tile reads half of a 256-token block).
+// Roles (448 threads):
 //   warp 0      producer: per 512-k segment, one bulk copy of the tile's packed
 //               weights (up to 16 KB, the tile-major layout); per 128-k step,
-//               one bulk copy per operand plane of the token tile's 32 KB block,
+//               one bulk copy per operand plane of the token tile's block (or half),
 //               already in the swizzled layout the MMA reads (act_ops.cuh).
 //               Copies are few and large because the copy engine's cost is per
 //               request, and per 128-byte row for tensor-map boxes.
-//   warp 1      allocates TMEM (512 columns: D = 256, A = 2 x 128); one lane
+//   warp 1      allocates TMEM (512 columns: D = TT, A = 2 x 128 at 256); one lane
 //               issues the MMAs: per 128-k step, 4 k32 steps x 2 planes.
 //   warps 2-5   decoders: thread = weight row; 2-bit codes -> e4m3 bytes by
 //               byte permutes, written to TMEM as the A operand (tcgen05.st),
@@ -55,12 +59,11 @@ namespace bitlinear {
 namespace {
 
 constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
-constexpr int kTileT = 256;                 // tokens per tile (MMA N)
+constexpr int kBlockT = 256;                // tokens per block of the operand layout
 constexpr int kThreads = 448;
-constexpr int kNSX = 3;                     // operand stages (128 k each)
+constexpr int kNSXMax = 6;                  // operand stages (128 k each): 3 x 64 KB or 6 x 32 KB
 constexpr int kNSW = 2;                     // weight stages (512 k each)
-constexpr int kXPlaneBytes = kTileT * 128;  // 32 KB
-constexpr int kXStageBytes = 2 * kXPlaneBytes;
+constexpr int kXBytes = 3 * 2 * kBlockT * 128;  // 192 KB of operand stages for either tile
 constexpr int kWStageBytes = 128 * 128;     // one segment: 128 rows x 128 bytes of packed codes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 256;             // A buffers at columns 256 and 384
@@ -69,9 +72,9 @@ constexpr uint32_t kCodeToE4M3 = 0x00B83800u;  // bytes 0x00 (code 0), 0x38 (+1)
 
 // shared memory (after 1024-byte alignment)
 constexpr int kOffX = 0;
-constexpr int kOffW = kOffX + kNSX * kXStageBytes;
+constexpr int kOffW = kOffX + kXBytes;
 constexpr int kOffBar = kOffW + kNSW * kWStageBytes;
-constexpr int kNumBars = 2 * kNSX + 2 * kNSW + 2 * 2 + 2 + 1;
+constexpr int kNumBars = 2 * kNSXMax + 2 * kNSW + 2 * 2 + 2 + 1;
 constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
 
 struct PrefillParams {
@@ -91,11 +94,12 @@ struct Bars {
   uint32_t full_x, empty_x, full_w, empty_w, a_full, a_empty, d_full, d_empty, fin;
 };
 
+template <int NSX>
 __device__ __forceinline__ Bars bars_at(uint32_t base) {
   Bars b;
   b.full_x = base;
-  b.empty_x = b.full_x + 8 * kNSX;
-  b.full_w = b.empty_x + 8 * kNSX;
+  b.empty_x = b.full_x + 8 * NSX;
+  b.full_w = b.empty_x + 8 * NSX;
   b.empty_w = b.full_w + 8 * kNSW;
   b.a_full = b.empty_w + 8 * kNSW;
   b.a_empty = b.a_full + 16;
@@ -135,14 +139,18 @@ __device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
 // tile: each copies 256 / CL token rows of every operand stage and multicasts
 // them to all CL, and each one's MMA completion releases the stage in all CL,
 // so the cluster reads the activations from L2 once instead of CL times.
-template <int CL>
+template <int CL, int TT>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p) {
+  constexpr int kNSX = 3 * kBlockT / TT;        // operand stages
+  constexpr int kXPlaneBytes = TT * 128;        // one plane of a stage: TT token rows x 128 k
+  constexpr int kXStageBytes = 2 * kXPlaneBytes;
+  constexpr int kTilesPerBlock = kBlockT / TT;  // token tiles per block of the operand layout
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   const uint32_t sbase = smem_u32(smem);
-  const Bars B = bars_at(sbase + kOffBar);
+  const Bars B = bars_at<kNSX>(sbase + kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -209,7 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
             mbar_arrive_expect_tx(B.full_x + 8 * xslot, (uint32_t)kXStageBytes);
             const uint32_t part = kXPlaneBytes / CL;            // this CTA's rows of the block
             const uint32_t dst = sbase + kOffX + xslot * kXStageBytes + rank * part;
-            const uint8_t* src = p.x_ops + (((int64_t)tt * (nseg * 4) + sg * 4 + kk) << 15) + rank * part;
+            const int blk = tt / kTilesPerBlock, sub = tt % kTilesPerBlock;
+            const uint8_t* src = p.x_ops + (((int64_t)blk * (nseg * 4) + sg * 4 + kk) << 15) +
+                                 sub * kXPlaneBytes + rank * part;
             if (CL > 1) {
               bulk_g2s_mc(dst, src, part, B.full_x + 8 * xslot, kMask);
               bulk_g2s_mc(dst + kXPlaneBytes, src + p.plane_bytes, part, B.full_x + 8 * xslot, kMask);
@@ -235,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      const uint32_t idesc = idesc_e4m3_f32(kTileW, kTileT);
+      const uint32_t idesc = idesc_e4m3_f32(kTileW, TT);
       int xs = 0, as = 0, tcount = 0;
       for (int ct = cid; ct < ctiles && !s_abort; ct += ncl, ++tcount) {
         if (tcount >= 1 && !wait_or_abort(B.d_empty, (tcount - 1) & 1, &s_abort, p.dev_err)) break;
@@ -320,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     // ------------------------------------------------------------ epilogue
     pdl_wait();                                // act_scale and y follow the stream order
     const int q4 = warp & 3;
-    const int half = (warp - 6) >> 2;          // tokens [128 half, 128 half + 128) of the tile
+    const int half = (warp - 6) >> 2;          // tokens [TT/2 half, TT/2 (half + 1)) of the tile
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
-    constexpr int kChunks = kTileT / 2 / 32;   // 4 chunks of 32 tokens
+    constexpr int kChunks = TT / 2 / 32;       // chunks of 32 tokens per warp
     const int out_mode = p.out_dtype;
     int tcount = 0;
     for (int ct = cid; ct < ctiles && !warp_aborted(&s_abort); ct += ncl, ++tcount) {
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       const int n = wb * kTileW + 32 * q4 + lane;
       const bool nv = n < p.N;
       const float wsn = nv ? __ldg(p.w_scale + n) : 0.0f;
-      const int m0 = tt * kTileT + half * (kTileT / 2);
+      const int m0 = tt * TT + half * (TT / 2);
       float as_lane[kChunks];
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
@@ -340,11 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       if (!warp_wait_or_abort(B.d_full, tcount & 1, &s_abort, p.dev_err)) break;
       tc_fence_after();
       uint32_t rv[2][32];
-      tmem_ld32(tmem + lane_addr + half * (kTileT / 2), rv[0]);
+      tmem_ld32(tmem + lane_addr + half * (TT / 2), rv[0]);
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
         tmem_wait_ld();
-        if (c + 1 < kChunks) tmem_ld32(tmem + lane_addr + half * (kTileT / 2) + 32 * (c + 1), rv[(c + 1) & 1]);
+        if (c + 1 < kChunks) tmem_ld32(tmem + lane_addr + half * (TT / 2) + 32 * (c + 1), rv[(c + 1) & 1]);
         const int mbase = m0 + 32 * c;
         const int jmax = nv ? min(32, p.M - mbase) : 0;       // tokens of this chunk that exist
         const size_t o0 = (size_t)mbase * p.N + n;
@@ -407,6 +417,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 
 }  // namespace
 
+// Tokens per tile: 128 when that takes less time in tile-rounds of the persistent
+// grid, a 128-token tile costing 0.74 of a 256-token one (measured on B300 over
+// 2B and 8B shapes at 256-2048 tokens: half the MMAs and operand bytes, but the
+// same weight decode and a fixed cost per tile).
+int prefill_tile_tokens(int64_t M, int64_t N, int sms) {
+  const int64_t nwb = (N + kTileW - 1) / kTileW;
+  const int64_t CL = nwb >= 2 ? 2 : 1;
+  const int64_t ncl = sms / CL > 0 ? sms / CL : 1;
+  const int64_t g = (nwb + CL - 1) / CL;
+  const int64_t r256 = (g * ((M + 255) / 256) + ncl - 1) / ncl;
+  const int64_t r128 = (g * ((M + 127) / 128) + ncl - 1) / ncl;
+  return 74 * r128 < 100 * r256 ? 128 : 256;
+}
+
 cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
                               const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
                               void* y, int32_t* acc_debug, int* dev_err, bool pdl,
@@ -414,6 +438,8 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
   const int64_t Kp = act_ops_kpad(K);
   const int64_t nwb = (N + kTileW - 1) / kTileW;
   const int CL = nwb >= 2 ? 2 : 1;             // measured: 2 beats 1 and 4
+  const int sms = num_sms();
+  const int TT = prefill_tile_tokens(M, N, sms);
   PrefillParams p = {};
   p.packed = packed;
   p.x_ops = x_ops;
@@ -430,19 +456,19 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
   p.nseg = (int)(Kp / 512);
   p.ntiles_n16 = (int)(N / 16);
   p.nwb = (int)((N + kTileW - 1) / kTileW);
-  p.ntok = (int)((M + kTileT - 1) / kTileT);
+  p.ntok = (int)((M + TT - 1) / TT);
   const int64_t tiles = (int64_t)p.nwb * p.ntok;
   if (tiles > (1LL << 30)) return cudaErrorInvalidValue;
   p.tiles = (int)tiles;
   static bool attr_set = false;
   if (!attr_set) {
-    for (void* f : {(void*)prefill_tc_kernel<1>, (void*)prefill_tc_kernel<2>, (void*)prefill_tc_kernel<4>}) {
+    for (void* f : {(void*)prefill_tc_kernel<1, 256>, (void*)prefill_tc_kernel<2, 256>,
+                    (void*)prefill_tc_kernel<1, 128>, (void*)prefill_tc_kernel<2, 128>}) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
     }
     attr_set = true;
   }
-  const int sms = num_sms();
   const int64_t ctiles = ((nwb + CL - 1) / CL) * p.ntok;
   int64_t clusters = sms / CL;
   if (clusters > ctiles) clusters = ctiles;
@@ -466,9 +492,13 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
   cfg.attrs = attr;
   cfg.numAttrs = na;
   cudaError_t e;
-  if (CL == 4) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<4>, p);
-  else if (CL == 2) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<2>, p);
-  else e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<1>, p);
+  if (TT == 128) {
+    if (CL == 2) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<2, 128>, p);
+    else e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<1, 128>, p);
+  } else {
+    if (CL == 2) e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<2, 256>, p);
+    else e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<1, 256>, p);
+  }
   count_launches(1);
   return e;
 }

@@ -286,13 +286,16 @@ def test_forward_from_quant_operands_matches_oracle(M, N, K, dt, pdl):
 
 
 @pytest.mark.parametrize("M,N,K,dt", [
+    # 128-token tiles (few tiles: more of them fill more SMs)
     (33, 48, 512, torch.float32),       # just above the decode limit; one partial weight block
-    (256, 160, 1024, torch.bfloat16),   # one full token tile
-    (300, 384, 2560, torch.float32),    # ragged second token tile
+    (256, 160, 1024, torch.bfloat16),   # both halves of one operand block
+    (300, 384, 2560, torch.float32),    # ragged third token tile
     (512, 256, 384, torch.bfloat16),    # K % 512 == 384: a zero-padded segment tail
     (80, 128, 14336, torch.float32),    # long K: |acc| up to 127 * 14336
-    (256, 19200, 512, torch.bfloat16),  # 75 tiles on 74 clusters: the last one split in 16 x 16 tokens
-    (300, 13824, 512, torch.float32),   # 108 tiles: the last wave in sub-tiles of 128 tokens
+    (600, 512, 1536, torch.bfloat16),   # five token tiles, the last one ragged and alone in its block
+    # 256-token tiles (enough tiles for whole waves)
+    (256, 19200, 512, torch.bfloat16),  # 75 cluster tiles on 74 clusters
+    (300, 13824, 512, torch.float32),   # 108 cluster tiles, the second token tile ragged
 ])
 def test_prefill_matches_oracle(M, N, K, dt):
     # M > 32 tokens run on the tcgen05 kernel (weights decoded into tensor memory)
