@@ -468,6 +468,7 @@ def our_arm(args):
             g.replay()
         stream.synchronize()
         fwd_ms = []            # per-launch ms, one entry per forward launch of a step
+        per_shape = []         # per (M, projection): launch time and algorithmic GB/s
         for M, p, g in fwd_graphs:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -477,6 +478,9 @@ def our_arm(args):
             stream.synchronize()
             per_launch = e0.elapsed_time(e1) / (args.steps * len(weights))
             fwd_ms.extend([per_launch] * len(weights))
+            alg = p.N * p.K // 4 + 2 * M * p.K + 4 * M + 4 * p.N + 2 * M * p.N
+            per_shape.append({"tokens": M, "projection": p.name, "launch_us": per_launch * 1e3,
+                              "alg_gbs": alg / (per_launch * 1e-3) / 1e9})
     alg_bytes_fwd = []
     for M, p, _ in fwd_graphs:
         for _ in weights:
@@ -581,7 +585,8 @@ def our_arm(args):
                 "timing": "CUDA events around K replays of a graph of the 30 layers' launches per (M, projection)",
                 "alg_bytes_per_launch": sum(alg_bytes_fwd) / len(alg_bytes_fwd),
                 "avg_launch_us": sum(fwd_ms) / len(fwd_ms) * 1e3,
-                "share_of_step": sum(fwd_ms) / ms if ms > 0 else None}
+                "share_of_step": sum(fwd_ms) / ms if ms > 0 else None,
+                "per_shape": per_shape}
 
     # ---- CPU baseline (rank 0, N = 1 only)
     prefill = None

@@ -135,12 +135,23 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
         gv_[i][hv] = (gain && tid + i * T < U && v < V) ? __ldg(gain + v) : kOnes;
       }
   }
+  // Pull the row into L2 before the wait.  A row that no earlier kernel writes
+  // (staged by a copy) then comes from L2 after the wait instead of HBM; a row that
+  // the previous kernel writes is updated in L2, the point of coherence, so the
+  // loads after the wait read its final values either way.
+  const uint4* xr = x + (size_t)row * ld;
+  if (!glu) {
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+      const int u = tid + i * T;
+      if (u < U && (u & 3) == 0) prefetch_l2(xr + 2 * u);   // one per 128-byte line
+    }
+  }
   // Let the next kernel launch now: it waits for this one to complete, and this one
   // completes only after the kernel before it (the wait below), so the next kernel
   // can set up and prefetch its weights while the previous one still runs.
   pdl_launch_dependents();
   pdl_wait();                                // x may be the previous kernel's output
-  const uint4* xr = x + (size_t)row * ld;
   const float* gr = glu ? glu + (size_t)row * 2 * K : nullptr;
 
   uint4 xv[UPT][2];
