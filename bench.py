@@ -257,14 +257,17 @@ def reference_arm(args):
 # our arm
 # ---------------------------------------------------------------------------
 
-def traffic_record(kernel_src: str):
-    """ncu DRAM bytes per launch recorded for the current source of the kernel, or None."""
+def traffic_record(kernel_srcs):
+    """ncu DRAM bytes per launch recorded for the current sources of the kernels, or None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path))
     except Exception:
         return None
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for src in kernel_srcs:
+        h.update(open(src, "rb").read())
+    sha = h.hexdigest()[:16]
     r = rec.get(WORKLOAD)
     if not r or r.get("source_sha") != sha:
         return None
@@ -389,18 +392,28 @@ def our_arm(args):
     stream = torch.cuda.Stream(device=dev)
     FL = bl.FLAG_PDL
 
+    def alg_bytes(M, p):
+        # packed weights, the activation codes (int8 on the code route, two e4m3 planes
+        # otherwise), scales, bf16 outputs
+        acts = M * p.K if M <= bl.CODES_MAX_M else 2 * M * p.K
+        return p.N * p.K // 4 + acts + 4 * M + 4 * p.N + 2 * M * p.N
+
+    def ops_for(M, K):
+        # the tensor-core operand form, for token counts the CUDA-core kernel does not take
+        return None if M <= bl.CODES_MAX_M else ops[(M, K)]
+
     def step():
         """One pass: for M in (1, 8), for every layer and projection: RMSNorm + int8
-        quantization (writing the tensor-core operand form) and the contraction."""
+        quantization and the contraction (on the int8 codes for M <= CODES_MAX_M, else on
+        the tensor-core operand form)."""
         for M in wl.tokens:
             for row in weights:
                 for (p, packed, w_scale) in row:
                     bl.bitlinear_quant_act(xs[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)],
-                                           act_scale=sc[(M, p.K)], x_ops=ops[(M, p.K)], flags=FL,
+                                           act_scale=sc[(M, p.K)], x_ops=ops_for(M, p.K), flags=FL,
                                            stream=stream)
-                    bl.bitlinear_forward(None, sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
-                                         y=ys[(M, p.N)], x_ops=ops[(M, p.K)], flags=FL, K=p.K,
-                                         stream=stream)
+                    bl.bitlinear_forward(xq[(M, p.K)], sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
+                                         y=ys[(M, p.N)], x_ops=ops_for(M, p.K), flags=FL, stream=stream)
 
     def barrier():
         if pg is not None:
@@ -455,9 +468,8 @@ def our_arm(args):
                 def fwd_only(M=M, pi=pi, p=p):
                     for row in weights:
                         _, packed, w_scale = row[pi]
-                        bl.bitlinear_forward(None, sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
-                                             y=ys[(M, p.N)], x_ops=ops[(M, p.K)], flags=FL, K=p.K,
-                                             stream=stream)
+                        bl.bitlinear_forward(xq[(M, p.K)], sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
+                                             y=ys[(M, p.N)], x_ops=ops_for(M, p.K), flags=FL, stream=stream)
                 fwd_only()
                 stream.synchronize()
                 g = torch.cuda.CUDAGraph()
@@ -478,13 +490,13 @@ def our_arm(args):
             stream.synchronize()
             per_launch = e0.elapsed_time(e1) / (args.steps * len(weights))
             fwd_ms.extend([per_launch] * len(weights))
-            alg = p.N * p.K // 4 + 2 * M * p.K + 4 * M + 4 * p.N + 2 * M * p.N
+            alg = alg_bytes(M, p)
             per_shape.append({"tokens": M, "projection": p.name, "launch_us": per_launch * 1e3,
                               "alg_gbs": alg / (per_launch * 1e-3) / 1e9})
     alg_bytes_fwd = []
     for M, p, _ in fwd_graphs:
         for _ in weights:
-            alg_bytes_fwd.append(p.N * p.K // 4 + 2 * M * p.K + 4 * M + 4 * p.N + 2 * M * p.N)
+            alg_bytes_fwd.append(alg_bytes(M, p))
     per_step_launches = len(alg_bytes_fwd)
 
     # ---- end to end through the public API: pinned host inputs in, bf16 outputs out.
@@ -543,9 +555,9 @@ def our_arm(args):
                     yo = out_off[(M, li, pi)]
                     y = dev_out[yo:yo + M * p.N].view(M, p.N)
                     bl.bitlinear_quant_act(x, gains[p.K], RMS_EPS, x_q=xq[(M, p.K)], act_scale=sc[(M, p.K)],
-                                           x_ops=ops[(M, p.K)], flags=FL, stream=stream)
-                    bl.bitlinear_forward(None, sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16, y=y,
-                                         x_ops=ops[(M, p.K)], flags=FL, K=p.K, stream=stream)
+                                           x_ops=ops_for(M, p.K), flags=FL, stream=stream)
+                    bl.bitlinear_forward(xq[(M, p.K)], sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16, y=y,
+                                         x_ops=ops_for(M, p.K), flags=FL, stream=stream)
                 done = torch.cuda.Event()
                 done.record(stream)
                 side.wait_event(done)
@@ -578,10 +590,12 @@ def our_arm(args):
     # ---- roofline of the dominant kernel (the contraction)
     hbm, bf16_tf, peak_src = measured_peaks()
     achieved = sum(alg_bytes_fwd) / (sum(fwd_ms) * 1e-3) / 1e9
-    traffic = traffic_record(os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc", "decode_tc.cu"))
+    csrc = os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc")
+    traffic = traffic_record([os.path.join(csrc, "decode_dp4a.cu"), os.path.join(csrc, "decode_tc.cu")])
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic, "peak_source": peak_src,
-                "kernel": "decode_tc_kernel (bitlinear_forward: ternary contraction + dequant, tcgen05)",
+                "kernel": "bitlinear_forward's decode contraction + dequant: decode_dp4a_kernel (int8 codes, "
+                          "CUDA cores) at M = 1, decode_tc_kernel (tcgen05) at M = 8",
                 "timing": "CUDA events around K replays of a graph of the 30 layers' launches per (M, projection)",
                 "alg_bytes_per_launch": sum(alg_bytes_fwd) / len(alg_bytes_fwd),
                 "avg_launch_us": sum(fwd_ms) / len(fwd_ms) * 1e3,

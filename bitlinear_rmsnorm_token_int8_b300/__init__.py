@@ -29,13 +29,16 @@ __all__ = [
     "bitlinear_forward_workspace_bytes", "bitlinear_pack_workspace_bytes", "OUT_F32", "OUT_BF16",
     "STATUS", "bitlinear_kernel_launches", "bitlinear_act_ops_bytes", "FLAG_PDL", "OUT_BF16_ADD",
     "bitlinear_block_forward", "bitlinear_block_workspace_bytes", "pack_stacked", "LAYER_FIELDS",
-    "bitlinear_linear_forward", "bitlinear_linear_workspace_bytes",
+    "bitlinear_linear_forward", "bitlinear_linear_workspace_bytes", "CODES_MAX_M",
 ]
 
 OUT_F32 = 0
 OUT_BF16 = 1
 OUT_BF16_ADD = 2
 FLAG_PDL = 1
+# BITLINEAR_CODES_MAX_M: bitlinear_forward given x_q contracts on the int8 codes (x_ops
+# unused, no workspace) for one token, and for two with K <= 4096 and N K <= 2^26
+CODES_MAX_M = 2
 STATUS = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_DTYPE", 5: "ERR_DEVICE",
           6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_WORKSPACE", 9: "ERR_NONFINITE", 10: "ERR_FLAGS"}
 
@@ -217,7 +220,8 @@ def bitlinear_forward(x_q, act_scale: torch.Tensor, packed: torch.Tensor,
         y = torch.empty((M, N), dtype=out_dtype, device=packed.device)
     if x_ops is None and workspace is None:
         need = bitlinear_forward_workspace_bytes(M, N, K)
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=packed.device)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=packed.device)
     _check("bitlinear_forward", lib().bitlinear_forward(
         _ptr(x_q), _ptr(act_scale), _ptr(x_ops), _ptr(packed), _ptr(w_scale), M, N, K, code, _ptr(y),
         _ptr(acc_debug), _ptr(workspace), 0 if workspace is None else workspace.numel(),

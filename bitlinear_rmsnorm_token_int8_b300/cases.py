@@ -1,12 +1,16 @@
 """Single-shape runs of the hot path, for profilers (ncu) and quick timing.
 
-    python -m bitlinear_rmsnorm_token_int8_b300.cases forward M K N [reps]
+    python -m bitlinear_rmsnorm_token_int8_b300.cases forward M K N [reps] [route]
         one BitLinear projection: quantize M x K activations once, then `reps`
-        contractions against one packed N x K weight (decode kernel for M <= 32,
-        tensor-core prefill kernel above).
+        contractions against one packed N x K weight.  route: `auto` (default: the
+        library's choice given both x_q and the operand form: the int8-code kernel
+        for one token (two with K <= 4096), the tcgen05 decode kernel up to 32
+        tokens, the tcgen05 prefill kernel above), `ops` (operand form only:
+        always a tcgen05 kernel) or `codes` (x_q only).
     python -m bitlinear_rmsnorm_token_int8_b300.cases shapes WORKLOAD [reps]
         every (tokens, projection) shape of a named workload (synth.WORKLOADS),
-        `reps` contractions each, every one on freshly packed weights (cold L2).
+        `reps` contractions each (route `auto`), every one on freshly packed
+        weights (cold L2).
 
 Inputs are seeded synthetic draws (synth); every call goes through the public
 binding, and the run ends by checking the device error word.
@@ -21,9 +25,13 @@ from . import bitlinear_forward, bitlinear_get_device_error, bitlinear_pack_weig
 from . import synth
 
 
-def _one(M: int, K: int, N: int, reps: int, dev, fresh_weights: bool) -> None:
+def _one(M: int, K: int, N: int, reps: int, dev, fresh_weights: bool, route: str = "auto") -> None:
     x = synth.activations(M, K, seed=synth.act_seed(7, M, K)).to(dev)
-    _, sc, ops = bitlinear_quant_act(x, None, 1e-5, x_ops=True)
+    xq, sc, ops = bitlinear_quant_act(x, None, 1e-5, x_ops=True)
+    if route == "ops":
+        xq = None
+    elif route == "codes":
+        ops = None
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     packed = ws = None
     for r in range(reps):
@@ -31,7 +39,7 @@ def _one(M: int, K: int, N: int, reps: int, dev, fresh_weights: bool) -> None:
             W = synth.latent_weights_device(N, K, seed=synth.weight_seed(7, r, 0), device=dev)
             packed, ws, _ = bitlinear_pack_weights(W)
             del W
-        bitlinear_forward(None, sc, packed, ws, y=y, x_ops=ops, K=K)
+        bitlinear_forward(xq, sc, packed, ws, y=y, x_ops=ops, K=K)
     torch.cuda.synchronize()
 
 
@@ -43,8 +51,12 @@ def main(argv: list[str]) -> int:
     if argv[0] == "forward":
         M, K, N = (int(a) for a in argv[1:4])
         reps = int(argv[4]) if len(argv) > 4 else 3
-        _one(M, K, N, reps, dev, fresh_weights=False)
-        print(f"forward M={M} K={K} N={N} x{reps}")
+        route = argv[5] if len(argv) > 5 else "auto"
+        if route not in ("auto", "ops", "codes"):
+            print(__doc__)
+            return 2
+        _one(M, K, N, reps, dev, fresh_weights=False, route=route)
+        print(f"forward M={M} K={K} N={N} x{reps} route={route}")
     else:
         wl = synth.WORKLOADS[argv[1]]
         reps = int(argv[2]) if len(argv) > 2 else 2

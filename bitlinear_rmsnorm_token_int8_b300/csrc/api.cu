@@ -162,6 +162,8 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return forward_workspace_bytes(M, N, K);
 }
 
+static_assert(kDp4aMaxM == BITLINEAR_CODES_MAX_M, "the header's CODES_MAX_M is the codes kernel's limit");
+
 bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, const void* x_ops,
                                    const uint8_t* packed, const float* w_scale, int64_t M,
                                    int64_t N, int64_t K, int out_dtype, void* y,
@@ -179,9 +181,9 @@ bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, co
       !aligned16(packed) || !aligned16(w_scale) || !aligned16(y) ||
       (acc_debug && !aligned16(acc_debug)))
     return BITLINEAR_ERR_ALIGN;
-  if (!x_ops) {
+  if (!x_ops) {                                   // x_q is converted in the workspace, if needed
     const size_t need = forward_workspace_bytes(M, N, K);
-    if (!workspace || workspace_bytes < need) return BITLINEAR_ERR_WORKSPACE;
+    if (need && (!workspace || workspace_bytes < need)) return BITLINEAR_ERR_WORKSPACE;
     if (!aligned16(workspace)) return BITLINEAR_ERR_ALIGN;
   }
   const DeviceState* dev = current_device();
@@ -229,6 +231,16 @@ bitlinear_status bitlinear_linear_forward(const void* x_bf16, const void* gain_b
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ops = static_cast<uint8_t*>(workspace);
   float* scale = act_scale ? act_scale : reinterpret_cast<float*>(ops + linear_ops_bytes(M, K));
+  if (codes_route(M, N, K)) {
+    // a few tokens: the contraction reads the int8 codes (kept in the workspace's
+    // operand region unless x_q is given), not the operand form
+    int8_t* codes = x_q ? x_q : reinterpret_cast<int8_t*>(ops);
+    cudaError_t e = launch_quant_act(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
+                                     rms_eps, M, K, codes, scale, nullptr, pdl, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(launch_forward(codes, scale, nullptr, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
+                                    nullptr, dev->err_word, true, s));
+  }
   cudaError_t e = launch_quant_act(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
                                    rms_eps, M, K, x_q, scale, ops, pdl, s);
   if (e != cudaSuccess) return from_cuda(e);

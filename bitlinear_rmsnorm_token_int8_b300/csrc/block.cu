@@ -85,26 +85,31 @@ extern "C" bitlinear_status bitlinear_block_forward(const bitlinear_layer* layer
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
   cudaError_t e = cudaSuccess;
-  auto quant = [&](const uint16_t* in, int64_t ld, const float* glu, const void* gain, int64_t K) {
+  // per projection: int8 codes in the operand region for the CUDA-core contraction
+  // (one or two tokens), or the tensor-core operand form
+  int8_t* const codes_buf = reinterpret_cast<int8_t*>(w.ops);
+  auto quant = [&](const uint16_t* in, int64_t ld, const float* glu, const void* gain, int64_t N, int64_t K) {
+    const bool codes = codes_route(M, N, K);
     if (e == cudaSuccess)
-      e = launch_quant_act_ex(in, ld, glu, static_cast<const uint16_t*>(gain), rms_eps, M, K, nullptr, w.scale,
-                              w.ops, pdl, s);
+      e = launch_quant_act_ex(in, ld, glu, static_cast<const uint16_t*>(gain), rms_eps, M, K,
+                              codes ? codes_buf : nullptr, w.scale, codes ? nullptr : w.ops, pdl, s);
     pdl = true;                         // everything after the first kernel is ours
   };
   auto forward = [&](const uint8_t* packed, const float* wscale, int64_t N, int64_t K, int out_dtype, void* y) {
+    const bool codes = codes_route(M, N, K);
     if (e == cudaSuccess)
-      e = launch_forward(nullptr, w.scale, w.ops, packed, wscale, M, N, K, out_dtype, y, nullptr, nullptr,
-                         err, true, s);
+      e = launch_forward(codes ? codes_buf : nullptr, w.scale, codes ? nullptr : w.ops, packed, wscale, M, N, K,
+                         out_dtype, y, nullptr, nullptr, err, true, s);
   };
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const bitlinear_layer& L = layers[l];
-    quant(x, H, nullptr, L.gain_qkv, H);
+    quant(x, H, nullptr, L.gain_qkv, NQKV, H);
     forward(L.qkv, L.qkv_scale, NQKV, H, BITLINEAR_OUT_BF16, w.qkv);
-    quant(w.qkv, NQKV, nullptr, L.gain_o, H);                  // the query slice stands in for attention
+    quant(w.qkv, NQKV, nullptr, L.gain_o, H, H);                  // the query slice stands in for attention
     forward(L.o, L.o_scale, H, H, BITLINEAR_OUT_BF16_ADD, x_bf16);
-    quant(x, H, nullptr, L.gain_gate_up, H);
+    quant(x, H, nullptr, L.gain_gate_up, 2 * F, H);
     forward(L.gate_up, L.gate_up_scale, 2 * F, H, BITLINEAR_OUT_F32, w.gu);
-    quant(nullptr, F, w.gu, L.gain_down, F);                   // h = bf16(relu(gate)^2 * up)
+    quant(nullptr, F, w.gu, L.gain_down, H, F);                   // h = bf16(relu(gate)^2 * up)
     forward(L.down, L.down_scale, H, F, BITLINEAR_OUT_BF16_ADD, x_bf16);
   }
   return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;

@@ -86,6 +86,17 @@ cudaError_t launch_decode_tc(const uint8_t* x_ops, const float* act_scale, const
                              void* y, int32_t* acc_debug, int* dev_err, bool pdl,
                              cudaStream_t stream);
 
+// Decode contraction for one or two tokens on the CUDA cores (int8 dot products),
+// reading the int8 codes x_q; shared memory per CTA from decode_dp4a_smem.
+constexpr int64_t kDp4aMaxM = 2;
+size_t decode_dp4a_smem(int64_t M, int64_t K);
+// True when bitlinear_forward with x_q takes that kernel: M == 1, or M == 2 with
+// K <= 4096 and N K <= 2^26, and the tokens' staged codes fit in shared memory.
+bool codes_route(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
+                               const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
+                               void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream);
+
 int num_sms();
 
 // ---- tensor maps and the prefill contraction ---------------------------------

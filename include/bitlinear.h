@@ -74,6 +74,18 @@ typedef enum bitlinear_status {
  */
 #define BITLINEAR_FLAG_PDL 1u
 
+/*
+ * Largest token count for which bitlinear_forward, given x_q, can contract on
+ * the int8 codes directly (a CUDA-core kernel with int8 dot products; x_ops is
+ * then not read and no workspace is needed): it does so for one token (any K)
+ * and for two tokens with K <= 4096 and N K <= 2^26 (at most 16 MiB of packed
+ * weights), the shapes where it was measured faster than the tensor-core
+ * kernel; bitlinear_forward_workspace_bytes returns 0 exactly then.  Otherwise,
+ * or with x_ops alone, the tensor-core kernels run on the operand form.
+ * Results are identical.
+ */
+#define BITLINEAR_CODES_MAX_M 2
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bitlinear_status_string(bitlinear_status status);
 
@@ -202,8 +214,9 @@ bitlinear_status bitlinear_quant_act(const void *x_bf16, const void *gain_bf16, 
 /* ------------------------------------------------------------------------ */
 
 /* Bytes of scratch that bitlinear_forward needs for this shape when it is called
- * with x_ops == NULL (it then converts x_q into the workspace first).  Called
- * with x_ops, it needs none. */
+ * with x_ops == NULL (it then converts x_q into the workspace first); 0 when the
+ * int8-code kernel takes x_q (see BITLINEAR_CODES_MAX_M).  Called with x_ops, it
+ * needs none. */
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -218,6 +231,7 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *           May be NULL when x_ops is given.
  * act_scale [M] fp32.
  * x_ops     the same codes in operand form (bitlinear_quant_act's x_ops), or NULL.
+ *           With x_q given and M <= BITLINEAR_CODES_MAX_M it is not read.
  * packed    [N,K/4] uint8 (from bitlinear_pack_weights).
  * w_scale   [N] fp32.
  * M, N, K   0 <= M <= 2^24 (M == 0 enqueues nothing and accepts NULL buffers),
@@ -227,8 +241,8 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * y         [M,N] out, fp32 or bf16.
  * acc_debug [M,N] int32 out with the raw accumulators, or NULL (for parity checks).
  * workspace >= bitlinear_forward_workspace_bytes(M,N,K) bytes of device scratch
- *           when x_ops is NULL (else unused, may be NULL).  Contents on entry do
- *           not matter.
+ *           when x_ops is NULL (may be NULL when that is 0, or with x_ops).
+ *           Contents on entry do not matter.
  * flags     0 or BITLINEAR_FLAG_PDL.
  *
  * Exactness: the kernels contract on the tensor cores with e4m3 operands; each

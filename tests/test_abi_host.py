@@ -43,6 +43,12 @@ def test_library_exports_every_declared_function(L):
         assert hasattr(L, n), f"{n} declared in include/ but not exported"
 
 
+def test_codes_route_limit_matches_the_header():
+    text = open(os.path.join(HEADER_DIR, "bitlinear.h")).read()
+    m = re.search(r"#define BITLINEAR_CODES_MAX_M (\d+)", text)
+    assert m and int(m.group(1)) == bl.CODES_MAX_M
+
+
 def test_status_strings_and_version(L):
     assert L.bitlinear_abi_version() == 1
     for s in range(11):
@@ -74,8 +80,9 @@ def test_forward_argument_errors(L):
     assert _fwd(L, x=None) == ERR_NULL
     assert _fwd(L, y=None) == ERR_NULL
     assert _fwd(L, flags=2) == ERR_FLAGS
-    assert _fwd(L, ws=None) == ERR_WS                        # no x_ops: x_q is converted in the workspace
-    assert _fwd(L, wsb=L.bitlinear_forward_workspace_bytes(4, 512, 256) - 1) == ERR_WS
+    # more than CODES_MAX_M tokens and no x_ops: x_q is converted in the workspace
+    assert _fwd(L, M=16, ws=None) == ERR_WS
+    assert _fwd(L, M=16, wsb=L.bitlinear_forward_workspace_bytes(16, 512, 256) - 1) == ERR_WS
     assert _fwd(L, ops=FAKE + 8) == ERR_ALIGN
     assert _fwd(L, M=0, x=None, y=None, s=None) == OK       # empty: nothing to touch
     assert _fwd(L, K=100) == ERR_SHAPE
@@ -92,6 +99,7 @@ def test_forward_argument_errors(L):
     if not torch.cuda.is_available():
         assert _fwd(L) == ERR_DEVICE
         assert _fwd(L, x=None, ops=FAKE, ws=None, flags=1) == ERR_DEVICE   # x_ops alone suffices
+        assert _fwd(L, M=2, ws=None) == ERR_DEVICE            # one or two tokens: x_q alone suffices
 
 
 def test_quant_act_argument_errors(L):

@@ -112,10 +112,12 @@ def test_linear_equals_quant_then_forward():
         assert torch.equal(xq1, xq2) and torch.equal(acc1, acc2) and torch.equal(y1, y2)
 
 
-def test_linear_residual_and_pdl_chain():
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_linear_residual_and_pdl_chain(M):
     # two layers back to back with programmatic dependent launch: the second reads the
-    # first's bf16 output (written by the kernel it overlaps with), then adds into a residual
-    M, H = 8, 2048
+    # first's bf16 output (written by the kernel it overlaps with), then adds into a
+    # residual; one and two tokens run on the int8-code kernel, eight on the tensor cores
+    H = 2048
     x = synth.activations(M, H, seed=91)
     g = synth.rms_gains(H, seed=92)
     W1 = synth.latent_weights(H, H, seed=93)

@@ -246,6 +246,31 @@ def test_forward_matches_oracle(M, N, K, dt):
     check_output(r)
 
 
+@pytest.mark.parametrize("M,K", [(1, 128), (1, 640), (2, 640), (1, 4096), (2, 4096), (1, 6912), (1, 14336),
+                                 (1, 65536)])
+def test_codes_route_equals_operand_route(M, K):
+    # one or two tokens given x_q run on the int8-code (CUDA-core) kernel; given only the
+    # operand form, on the tensor cores: same accumulators and outputs, both equal to the
+    # oracle's (N = 272: a second weight tile of 16 rows)
+    N = 272
+    x = synth.activations(M, K, seed=M + K)
+    W = synth.latent_weights(N, K, seed=K + 3)
+    packed, w_scale, gamma = bl.bitlinear_pack_weights(W.cuda())
+    xq, sc, ops = bl.bitlinear_quant_act(x.cuda(), None, RMS_EPS, x_ops=True)
+    assert bl.bitlinear_forward_workspace_bytes(M, N, K) == 0          # the codes route needs none
+    for dt in (torch.float32, torch.bfloat16):
+        acc1 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        acc2 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        y1 = bl.bitlinear_forward(xq, sc, packed, w_scale, out_dtype=dt, acc_debug=acc1, flags=bl.FLAG_PDL)
+        y2 = bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=dt, acc_debug=acc2, x_ops=ops, K=K)
+        torch.cuda.synchronize()
+        assert torch.equal(acc1, acc2) and torch.equal(y1, y2)
+    o_xq, _ = oracle.act_quant(synth.bf16_bits(x), None, RMS_EPS)
+    _, _, o_wq = oracle.pack_weights(W.numpy())
+    assert (xq.cpu().numpy() == o_xq).all()
+    assert (acc1.cpu().numpy() == oracle.ternary_matmul(o_xq, o_wq)).all()
+
+
 def test_forward_every_decode_m():
     # every token count the decode kernel takes (1..32: 8-token groups and their ragged ends)
     for M in range(1, 33):
