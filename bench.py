@@ -6,8 +6,9 @@ BitNet b1.58 (hidden 2560, FFN 6912; QKV 2560->3840, O 2560->2560, gate+up
 2560->2x6912, down 6912->2560) at M = 1 and M = 8 tokens, over 30 layers of
 distinct weights (520 MB of packed weights per pass, more than 4x the 126 MB
 L2, so no pass is served from L2).  One step = for M in (1, 8): for each layer
-and projection: RMSNorm + int8 quantization of the input, then the ternary
-contraction with fused dequantization (bitlinear_quant_act + bitlinear_forward).
+and projection: the BitLinear layer through the one-call API
+bitlinear_linear_forward (RMSNorm + int8 quantization of the input, the ternary
+contraction with fused dequantization; one kernel at M = 1, two at M = 8).
 Weights are packed once before timing (offline step).
 
 Metric: packed-weight GB/s (packed bytes streamed per step / step time).  The
@@ -375,7 +376,7 @@ def our_arm(args):
 
     # ---- activations and buffers
     Ks = sorted({p.K for p in wl.projections})
-    xs, gains, xq, sc, ops, ys = {}, {}, {}, {}, {}, {}
+    xs, gains, xq, sc, ops, ys, lws = {}, {}, {}, {}, {}, {}, {}
     for K in Ks:
         gains[K] = synth.rms_gains(K, synth.gain_seed(wl.seed, 0, K)).to(dev)
     for M in wl.tokens:
@@ -386,34 +387,39 @@ def our_arm(args):
             ops[(M, K)] = torch.empty(bl.bitlinear_act_ops_bytes(M, K), dtype=torch.uint8, device=dev)
         for p in wl.projections:
             ys[(M, p.N)] = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+            lws[(M, p.N, p.K)] = torch.empty(max(16, bl.bitlinear_linear_workspace_bytes(M, p.N, p.K)),
+                                             dtype=torch.uint8, device=dev)
 
     packed_bytes_step = sum(p.N * p.K // 4 for _ in wl.tokens for row in weights for (p, _, _) in row)
 
     stream = torch.cuda.Stream(device=dev)
     FL = bl.FLAG_PDL
 
+    def route(M, p):
+        return bl.bitlinear_linear_route(M, p.N, p.K)
+
     def alg_bytes(M, p):
-        # packed weights, the activation codes (int8 on the code route, two e4m3 planes
-        # otherwise), scales, bf16 outputs
-        acts = M * p.K if M <= bl.CODES_MAX_M else 2 * M * p.K
+        # per launch of the kernel timed for the roofline: packed weights, its activation
+        # input (bf16 x and gain for the one-token layer kernel, int8 codes for the code
+        # kernel, two e4m3 planes for tcgen05), scales, bf16 outputs
+        r = route(M, p)
+        acts = (2 * M * p.K + 2 * p.K if r == bl.ROUTE_FUSED else M * p.K if r == bl.ROUTE_CODES
+                else 2 * M * p.K)
         return p.N * p.K // 4 + acts + 4 * M + 4 * p.N + 2 * M * p.N
 
-    def ops_for(M, K):
-        # the tensor-core operand form, for token counts the CUDA-core kernel does not take
-        return None if M <= bl.CODES_MAX_M else ops[(M, K)]
+    def layer(M, x, p, packed, w_scale, y):
+        # one BitLinear layer through the public one-call API (RMSNorm + quantization +
+        # contraction): one kernel for one token, quantization + contraction otherwise
+        bl.bitlinear_linear_forward(x, gains[p.K], RMS_EPS, packed, w_scale, out_dtype=torch.bfloat16, y=y,
+                                    workspace=lws[(M, p.N, p.K)], flags=FL, stream=stream)
 
     def step():
-        """One pass: for M in (1, 8), for every layer and projection: RMSNorm + int8
-        quantization and the contraction (on the int8 codes for M <= CODES_MAX_M, else on
-        the tensor-core operand form)."""
+        """One pass: for M in (1, 8), for every layer and projection, the BitLinear layer
+        (bitlinear_linear_forward: RMSNorm, int8 quantization and the contraction)."""
         for M in wl.tokens:
             for row in weights:
                 for (p, packed, w_scale) in row:
-                    bl.bitlinear_quant_act(xs[(M, p.K)], gains[p.K], RMS_EPS, x_q=xq[(M, p.K)],
-                                           act_scale=sc[(M, p.K)], x_ops=ops_for(M, p.K), flags=FL,
-                                           stream=stream)
-                    bl.bitlinear_forward(xq[(M, p.K)], sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
-                                         y=ys[(M, p.N)], x_ops=ops_for(M, p.K), flags=FL, stream=stream)
+                    layer(M, xs[(M, p.K)], p, packed, w_scale, ys[(M, p.N)])
 
     def barrier():
         if pg is not None:
@@ -456,11 +462,18 @@ def our_arm(args):
     ms = max_over_ranks(start.elapsed_time(end) / args.steps, pg, dev)
     value = aggregate_gbs(world, packed_bytes_step, ms)
 
-    # ---- per-launch durations of the contraction kernel.  For each (M, projection) a
-    #      CUDA graph holds the 30 layers' forward launches back to back (distinct weights,
-    #      chained by programmatic dependent launch as in the step); CUDA events on the
-    #      launching stream bracket K replays, so the average is the kernel's duration in
-    #      a stream of launches, not host launch latency.
+    # ---- per-launch durations of the contraction kernel (for one token the layer kernel,
+    #      which also quantizes).  For each (M, projection) a CUDA graph holds the 30
+    #      layers' launches back to back (distinct weights, chained by programmatic
+    #      dependent launch as in the step); CUDA events on the launching stream bracket K
+    #      replays, so the average is the kernel's duration in a stream of launches, not
+    #      host launch latency.  Codes, scales and operand planes for the contraction-only
+    #      launches come from one quantization per (M, K) beforehand.
+    with torch.cuda.stream(stream):
+        for M in wl.tokens:
+            for K in Ks:
+                bl.bitlinear_quant_act(xs[(M, K)], gains[K], RMS_EPS, x_q=xq[(M, K)], act_scale=sc[(M, K)],
+                                       x_ops=ops[(M, K)], stream=stream)
     fwd_graphs = []
     with torch.cuda.stream(stream):
         for M in wl.tokens:
@@ -468,8 +481,14 @@ def our_arm(args):
                 def fwd_only(M=M, pi=pi, p=p):
                     for row in weights:
                         _, packed, w_scale = row[pi]
-                        bl.bitlinear_forward(xq[(M, p.K)], sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16,
-                                             y=ys[(M, p.N)], x_ops=ops_for(M, p.K), flags=FL, stream=stream)
+                        if route(M, p) == bl.ROUTE_FUSED:    # the layer is one kernel
+                            layer(M, xs[(M, p.K)], p, packed, w_scale, ys[(M, p.N)])
+                        else:                                  # the contraction kernel alone
+                            codes = route(M, p) == bl.ROUTE_CODES
+                            bl.bitlinear_forward(xq[(M, p.K)] if codes else None, sc[(M, p.K)], packed, w_scale,
+                                                 out_dtype=torch.bfloat16, y=ys[(M, p.N)],
+                                                 x_ops=None if codes else ops[(M, p.K)], K=p.K, flags=FL,
+                                                 stream=stream)
                 fwd_only()
                 stream.synchronize()
                 g = torch.cuda.CUDAGraph()
@@ -554,10 +573,7 @@ def our_arm(args):
                     x = dev_in[o:o + M * p.K].view(M, p.K)
                     yo = out_off[(M, li, pi)]
                     y = dev_out[yo:yo + M * p.N].view(M, p.N)
-                    bl.bitlinear_quant_act(x, gains[p.K], RMS_EPS, x_q=xq[(M, p.K)], act_scale=sc[(M, p.K)],
-                                           x_ops=ops_for(M, p.K), flags=FL, stream=stream)
-                    bl.bitlinear_forward(xq[(M, p.K)], sc[(M, p.K)], packed, w_scale, out_dtype=torch.bfloat16, y=y,
-                                         x_ops=ops_for(M, p.K), flags=FL, stream=stream)
+                    layer(M, x, p, packed, w_scale, y)
                 done = torch.cuda.Event()
                 done.record(stream)
                 side.wait_event(done)
@@ -591,11 +607,13 @@ def our_arm(args):
     hbm, bf16_tf, peak_src = measured_peaks()
     achieved = sum(alg_bytes_fwd) / (sum(fwd_ms) * 1e-3) / 1e9
     csrc = os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc")
-    traffic = traffic_record([os.path.join(csrc, "decode_dp4a.cu"), os.path.join(csrc, "decode_tc.cu")])
+    traffic = traffic_record([os.path.join(csrc, "decode_dp4a.cu"), os.path.join(csrc, "quant_math.cuh"),
+                              os.path.join(csrc, "decode_tc.cu")])
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic, "peak_source": peak_src,
-                "kernel": "bitlinear_forward's decode contraction + dequant: decode_dp4a_kernel (int8 codes, "
-                          "CUDA cores) at M = 1, decode_tc_kernel (tcgen05) at M = 8",
+                "kernel": "the decode contraction + dequant of each projection: at M = 1 linear_dp4a_kernel "
+                          "(the whole layer: RMSNorm, quantization, int8-code contraction, CUDA cores), at "
+                          "M = 8 decode_tc_kernel (tcgen05)",
                 "timing": "CUDA events around K replays of a graph of the 30 layers' launches per (M, projection)",
                 "alg_bytes_per_launch": sum(alg_bytes_fwd) / len(alg_bytes_fwd),
                 "avg_launch_us": sum(fwd_ms) / len(fwd_ms) * 1e3,

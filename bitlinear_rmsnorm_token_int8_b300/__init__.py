@@ -29,7 +29,8 @@ __all__ = [
     "bitlinear_forward_workspace_bytes", "bitlinear_pack_workspace_bytes", "OUT_F32", "OUT_BF16",
     "STATUS", "bitlinear_kernel_launches", "bitlinear_act_ops_bytes", "FLAG_PDL", "OUT_BF16_ADD",
     "bitlinear_block_forward", "bitlinear_block_workspace_bytes", "pack_stacked", "LAYER_FIELDS",
-    "bitlinear_linear_forward", "bitlinear_linear_workspace_bytes", "CODES_MAX_M",
+    "bitlinear_linear_forward", "bitlinear_linear_workspace_bytes", "CODES_MAX_M", "bitlinear_linear_route",
+    "ROUTE_FUSED", "ROUTE_CODES", "ROUTE_DECODE", "ROUTE_PREFILL",
 ]
 
 OUT_F32 = 0
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.bitlinear_block_forward.restype = I
         L.bitlinear_linear_workspace_bytes.argtypes = [I64, I64, I64]
         L.bitlinear_linear_workspace_bytes.restype = SZ
+        L.bitlinear_linear_route.argtypes = [I64, I64, I64]
+        L.bitlinear_linear_route.restype = I
         L.bitlinear_linear_forward.argtypes = [P, P, F, P, P, I64, I64, I64, I, P, P, P, P, P, SZ, U, P]
         L.bitlinear_linear_forward.restype = I
         _lib = L
@@ -231,6 +234,14 @@ def bitlinear_forward(x_q, act_scale: torch.Tensor, packed: torch.Tensor,
 
 def bitlinear_linear_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(lib().bitlinear_linear_workspace_bytes(M, N, K))
+
+
+ROUTE_FUSED, ROUTE_CODES, ROUTE_DECODE, ROUTE_PREFILL = 0, 1, 2, 3
+
+
+def bitlinear_linear_route(M: int, N: int, K: int) -> int:
+    """Which kernels bitlinear_linear_forward runs for this shape (ROUTE_*; -1: rejected)."""
+    return int(lib().bitlinear_linear_route(M, N, K))
 
 
 def bitlinear_linear_forward(x: torch.Tensor, gain, rms_eps: float, packed: torch.Tensor,

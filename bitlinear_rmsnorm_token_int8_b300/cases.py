@@ -6,10 +6,13 @@
         library's choice given both x_q and the operand form: the int8-code kernel
         for one token (two with K <= 4096), the tcgen05 decode kernel up to 32
         tokens, the tcgen05 prefill kernel above), `ops` (operand form only:
-        always a tcgen05 kernel) or `codes` (x_q only).
+        always a tcgen05 kernel), `codes` (x_q only) or `layer` (the one-call
+        layer bitlinear_linear_forward on the bf16 activations: for one token
+        with K <= 8192 a single kernel that also quantizes).
     python -m bitlinear_rmsnorm_token_int8_b300.cases shapes WORKLOAD [reps]
         every (tokens, projection) shape of a named workload (synth.WORKLOADS),
-        `reps` contractions each (route `auto`), every one on freshly packed
+        `reps` launches each of the kernel bench.py times for it (route `layer`
+        where the layer is one kernel, else `auto`), every one on freshly packed
         weights (cold L2).
 
 Inputs are seeded synthetic draws (synth); every call goes through the public
@@ -21,7 +24,8 @@ import sys
 
 import torch
 
-from . import bitlinear_forward, bitlinear_get_device_error, bitlinear_pack_weights, bitlinear_quant_act
+from . import (ROUTE_FUSED, bitlinear_forward, bitlinear_get_device_error, bitlinear_linear_forward,
+               bitlinear_linear_route, bitlinear_pack_weights, bitlinear_quant_act)
 from . import synth
 
 
@@ -39,7 +43,10 @@ def _one(M: int, K: int, N: int, reps: int, dev, fresh_weights: bool, route: str
             W = synth.latent_weights_device(N, K, seed=synth.weight_seed(7, r, 0), device=dev)
             packed, ws, _ = bitlinear_pack_weights(W)
             del W
-        bitlinear_forward(xq, sc, packed, ws, y=y, x_ops=ops, K=K)
+        if route == "layer":
+            bitlinear_linear_forward(x, None, 1e-5, packed, ws, y=y)
+        else:
+            bitlinear_forward(xq, sc, packed, ws, y=y, x_ops=ops, K=K)
     torch.cuda.synchronize()
 
 
@@ -52,7 +59,7 @@ def main(argv: list[str]) -> int:
         M, K, N = (int(a) for a in argv[1:4])
         reps = int(argv[4]) if len(argv) > 4 else 3
         route = argv[5] if len(argv) > 5 else "auto"
-        if route not in ("auto", "ops", "codes"):
+        if route not in ("auto", "ops", "codes", "layer"):
             print(__doc__)
             return 2
         _one(M, K, N, reps, dev, fresh_weights=False, route=route)
@@ -62,7 +69,8 @@ def main(argv: list[str]) -> int:
         reps = int(argv[2]) if len(argv) > 2 else 2
         for M in wl.tokens:
             for p in wl.projections:
-                _one(M, p.K, p.N, reps, dev, fresh_weights=True)
+                route = "layer" if bitlinear_linear_route(M, p.N, p.K) == ROUTE_FUSED else "auto"
+                _one(M, p.K, p.N, reps, dev, fresh_weights=True, route=route)
                 print(f"shape M={M} {p.name} K={p.K} N={p.N} x{reps}")
     err = bitlinear_get_device_error()
     if err != 0:

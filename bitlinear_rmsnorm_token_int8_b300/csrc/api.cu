@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "../../include/bitlinear.h"
+#include "act_ops.cuh"
 #include "internal.h"
 
 namespace bitlinear {
@@ -206,6 +207,15 @@ size_t bitlinear_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return linear_split_bytes(M, K);
 }
 
+int bitlinear_linear_route(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || M > (int64_t(1) << 24) || N < 16 || N % 16 != 0 || N > (int64_t(1) << 24) || K < 128 ||
+      K % 128 != 0 || K > 65536)
+    return -1;
+  if (fused_route(M, N, K)) return BITLINEAR_ROUTE_FUSED;
+  if (codes_route(M, N, K)) return BITLINEAR_ROUTE_CODES;
+  return act_ops_prefill(M) ? BITLINEAR_ROUTE_PREFILL : BITLINEAR_ROUTE_DECODE;
+}
+
 bitlinear_status bitlinear_linear_forward(const void* x_bf16, const void* gain_bf16, float rms_eps,
                                           const uint8_t* packed, const float* w_scale, int64_t M,
                                           int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
@@ -231,6 +241,10 @@ bitlinear_status bitlinear_linear_forward(const void* x_bf16, const void* gain_b
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ops = static_cast<uint8_t*>(workspace);
   float* scale = act_scale ? act_scale : reinterpret_cast<float*>(ops + linear_ops_bytes(M, K));
+  if (fused_route(M, N, K))                      // one token: the whole layer in one kernel
+    return from_cuda(launch_linear_dp4a(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
+                                        rms_eps, packed, w_scale, N, K, out_dtype, y, x_q, act_scale, acc_debug,
+                                        pdl, s));
   if (codes_route(M, N, K)) {
     // a few tokens: the contraction reads the int8 codes (kept in the workspace's
     // operand region unless x_q is given), not the operand form

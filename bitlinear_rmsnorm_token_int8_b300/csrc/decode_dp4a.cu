@@ -29,6 +29,7 @@
 #include "act_ops.cuh"
 #include "device_util.cuh"
 #include "internal.h"
+#include "quant_math.cuh"
 
 namespace bitlinear {
 namespace {
@@ -37,6 +38,7 @@ constexpr int kDThreads = 128;               // 4 warps
 constexpr int kChunkPitch = 80;              // a staged 64-byte chunk + 16 bytes: conflict-free reads
 constexpr int kSegPitch = 8 * kChunkPitch;   // one token's 512 inputs in shared memory
 constexpr uint32_t kCodeToI8 = 0x00FF0100u;  // bytes 0x00 (code 0), 0x01 (+1), 0xFF (-1)
+constexpr int kFusedMaxSeg = 16;             // the one-token layer kernel: K <= 8192
 
 struct DecodeDp4aParams {
   const uint8_t* packed;
@@ -191,6 +193,165 @@ cudaError_t launch_mt(const DecodeDp4aParams& p, int KS, size_t smem, bool pdl, 
   return launch_ks<MT, 1>(p, smem, pdl, stream);
 }
 
+// ---- the whole layer for one token: RMSNorm + quantization + contraction --------
+// Every CTA forms the token's statistics itself (max|x g| and the pair sum of x^2)
+// with the thread-to-input mapping and reduction tree of quant_act_kernel for one
+// row (thread u takes inputs 16u..16u+15; its warps past the row add zeros, which
+// leaves the tree's result unchanged), so codes and scale equal that kernel's bit
+// for bit; the codes then go straight into the staging of the contraction.  CTA 0
+// also writes x_q and act_scale when asked for.  T = blockDim.x >= Kp / 16.
+
+struct LinearDp4aParams {
+  const uint4* x;            // bf16 row, 8 per vector
+  const uint4* gain;         // bf16 [K] or null
+  float rms_eps;
+  const uint8_t* packed;
+  const float* w_scale;
+  void* y;
+  int8_t* x_q;               // [K] out, or null
+  float* act_scale;          // [1] out, or null
+  int32_t* acc_debug;
+  int N, K, nseg, Np, out_dtype;
+};
+
+template <int KS, int PRE>
+__global__ void __launch_bounds__(512) linear_dp4a_kernel(const LinearDp4aParams p) {
+  __shared__ __align__(16) uint8_t xsm[kFusedMaxSeg * kSegPitch];
+  __shared__ float s_max[32];
+  __shared__ float2 s_ss[32];
+  __shared__ float s_m, s_sum;
+  constexpr int kRowsPerWarp = 4 / KS;
+  constexpr int kLog2KS = KS == 1 ? 0 : KS == 2 ? 1 : 2;
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int c = lane & 7;
+  const int ks = (lane >> 3) & (KS - 1);
+  const int row = (blockIdx.x * (T >> 5) + warp) * kRowsPerWarp + (lane >> (3 + kLog2KS));
+  const bool rv = row < p.Np;                                    // the last CTA may reach past Np
+  const int tile = row >> 7, r = row & 127;
+  const int R = min(128, p.Np - tile * 128);
+  const uint8_t* wrow = p.packed + (size_t)tile * p.nseg * 16384 + (size_t)r * 128 + ((c ^ (r & 7)) << 4);
+  const size_t seg_step = (size_t)R * 128;
+  uint4 wreg[PRE];
+#pragma unroll
+  for (int i = 0; i < PRE; ++i) {
+    const int s = ks + KS * i;
+    wreg[i] = (rv && s < p.nseg) ? __ldg(reinterpret_cast<const uint4*>(wrow + s * seg_step))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const bool nv = row < p.N;
+  const float wsn = nv ? __ldg(p.w_scale + row) : 0.0f;
+  // this thread's unit of the token: inputs 16 tid .. 16 tid + 15 (vectors 2 tid, 2 tid + 1)
+  const int V = p.K >> 3, U = (V + 1) >> 1;
+  uint4 gv[2];
+#pragma unroll
+  for (int hv = 0; hv < 2; ++hv) {
+    const int v = 2 * tid + hv;
+    gv[hv] = (p.gain && tid < U && v < V) ? __ldg(p.gain + v) : kOnes;
+  }
+  if (tid < U && (tid & 3) == 0) prefetch_l2(p.x + 2 * tid);
+  pdl_launch_dependents();
+  pdl_wait();                                // x and y follow the stream order
+
+  const bool out = nv && ks == 0 && c == 0;
+  float res = 0.0f;
+  if (out && p.out_dtype == 2)
+    res = __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(p.y) + row) << 16);
+
+  // statistics, as quant_act_kernel
+  uint4 xv[2];
+  float amax = 0.0f, hi = 0.0f, lo = 0.0f;
+#pragma unroll
+  for (int hv = 0; hv < 2; ++hv) {
+    const int v = 2 * tid + hv;
+    if (tid < U && v < V) {
+      xv[hv] = __ldcg(p.x + v);
+      float xf[8], gf[8];
+      unpack8(xv[hv], xf);
+      unpack8(gv[hv], gf);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        amax = fmaxf(amax, fabsf(__fmul_rn(xf[j], gf[j])));
+        float s_, e_;
+        two_sum(hi, __fmul_rn(xf[j], xf[j]), s_, e_);
+        hi = s_;
+        lo = __fadd_rn(lo, e_);
+      }
+    } else {
+      xv[hv] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  block_stats(amax, hi, lo, tid, T >> 5, s_max, s_ss, &s_m, &s_sum);
+  const float m = fmaxf(s_m, 1e-8f);
+  const float sq = __fdiv_rn(127.0f, m);
+  const float sigma = act_sigma(m, s_sum, p.K, p.rms_eps);
+
+  // codes of this unit (zero past K), staged permuted for the dot products
+  if (tid < p.nseg * 32) {
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int hv = 0; hv < 2; ++hv) {
+      float xf[8], gf[8];
+      unpack8(xv[hv], xf);
+      unpack8(gv[hv], gf);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int q = quant_code(__fmul_rn(xf[j], gf[j]), sq, m);
+        w[2 * hv + (j >> 2)] |= (uint32_t)(q & 0xff) << (8 * (j & 3));
+      }
+    }
+    const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
+    const int s = tid >> 5, cc = (tid >> 2) & 7, j = tid & 3;
+    *reinterpret_cast<uint4*>(xsm + s * kSegPitch + cc * kChunkPitch + 16 * j) = permute16(codes);
+    if (blockIdx.x == 0 && p.x_q && tid < U) *reinterpret_cast<uint4*>(p.x_q + 16 * tid) = codes;
+  }
+  if (blockIdx.x == 0 && tid == 0 && p.act_scale) *p.act_scale = sigma;
+  __syncthreads();
+
+  int acc[1] = {0};
+  const uint32_t xs = smem_u32(xsm) + c * kChunkPitch;
+#pragma unroll
+  for (int i = 0; i < PRE; ++i) {
+    const int s = ks + KS * i;
+    if (s < p.nseg) dot_chunk<1>(wreg[i], xs + s * kSegPitch, 0u, acc);
+  }
+  for (int s = ks + KS * PRE; s < p.nseg; s += KS)
+    dot_chunk<1>(rv ? __ldg(reinterpret_cast<const uint4*>(wrow + s * seg_step)) : make_uint4(0u, 0u, 0u, 0u),
+                 xs + s * kSegPitch, 0u, acc);
+  int v = acc[0];
+#pragma unroll
+  for (int o = 1; o < 8 * KS; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (!out) return;
+  const float yv = __fmul_rn(__fmul_rn((float)v, sigma), wsn);
+  if (p.out_dtype == 0) reinterpret_cast<float*>(p.y)[row] = yv;
+  else if (p.out_dtype == 1) reinterpret_cast<__nv_bfloat16*>(p.y)[row] = __float2bfloat16_rn(yv);
+  else reinterpret_cast<__nv_bfloat16*>(p.y)[row] = __float2bfloat16_rn(__fadd_rn(res, yv));
+  if (p.acc_debug) p.acc_debug[row] = v;
+}
+
+template <int KS, int PRE>
+cudaError_t launch_fused_cfg(const LinearDp4aParams& p, int T, bool pdl, cudaStream_t stream) {
+  const int rows = (T / 32) * 4 / KS;                            // weight rows per CTA
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.Np + rows - 1) / rows), 1, 1);
+  cfg.blockDim = dim3((unsigned)T, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, linear_dp4a_kernel<KS, PRE>, p);
+}
+
+template <int KS>
+cudaError_t launch_fused_ks(const LinearDp4aParams& p, int T, bool pdl, cudaStream_t stream) {
+  const int per_lane = (p.nseg + KS - 1) / KS;
+  return per_lane <= 4 ? launch_fused_cfg<KS, 4>(p, T, pdl, stream)
+       : per_lane <= 6 ? launch_fused_cfg<KS, 6>(p, T, pdl, stream)
+                       : launch_fused_cfg<KS, 8>(p, T, pdl, stream);
+}
+
 }  // namespace
 
 size_t decode_dp4a_smem(int64_t M, int64_t K) {
@@ -212,6 +373,42 @@ int dp4a_split(int nseg) {
   int ks = 1;
   while (ks < 4 && (nseg + ks - 1) / ks > 5) ks *= 2;
   return ks;
+}
+
+bool fused_route(int64_t M, int64_t N, int64_t K) {
+  return M == 1 && K <= kFusedMaxSeg * 512 && codes_route(M, N, K);
+}
+
+cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rms_eps, const uint8_t* packed,
+                               const float* w_scale, int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
+                               float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream) {
+  if (!fused_route(1, N, K)) return cudaErrorInvalidValue;
+  LinearDp4aParams p = {};
+  p.x = reinterpret_cast<const uint4*>(x);
+  p.gain = reinterpret_cast<const uint4*>(gain);
+  p.rms_eps = rms_eps;
+  p.packed = packed;
+  p.w_scale = w_scale;
+  p.y = y;
+  p.x_q = x_q;
+  p.act_scale = act_scale;
+  p.acc_debug = acc_debug;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.nseg = (int)(act_ops_kpad(K) / 512);
+  p.Np = (int)packed_rows(N);
+  p.out_dtype = out_dtype;
+  // threads: quant_act_kernel's for this row (one per 16 inputs, in whole warps),
+  // rounded up to whole 4-warp groups of rows
+  const int tq = (int)((K / 16 + 31) / 32 * 32);
+  const int T = (tq + 127) / 128 * 128;
+  const int KS = dp4a_split(p.nseg);
+  cudaError_t e;
+  if (KS == 4) e = launch_fused_ks<4>(p, T, pdl, stream);
+  else if (KS == 2) e = launch_fused_ks<2>(p, T, pdl, stream);
+  else e = launch_fused_ks<1>(p, T, pdl, stream);
+  count_launches(1);
+  return e;
 }
 
 cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const uint8_t* packed,

@@ -97,6 +97,13 @@ cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const 
                                const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
                                void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream);
 
+// The whole layer (RMSNorm + quantization + contraction) for one token in one kernel,
+// when K <= 8192 and the codes route applies; x_q and act_scale outputs optional.
+bool fused_route(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rms_eps, const uint8_t* packed,
+                               const float* w_scale, int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
+                               float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream);
+
 int num_sms();
 
 // ---- tensor maps and the prefill contraction ---------------------------------

@@ -31,57 +31,10 @@
 #include "act_ops.cuh"
 #include "device_util.cuh"
 #include "internal.h"
+#include "quant_math.cuh"
 
 namespace bitlinear {
 namespace {
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
-// Exactly rounded code of 127*p/m (ties to even), see the file comment.
-__device__ __forceinline__ int quant_code(float p, float s, float m) {
-  const float t = __fmul_rn(p, s);
-  const float f = floorf(t);
-  const float dist = fabsf(__fsub_rn(t, __fadd_rn(f, 0.5f)));
-  float q;
-  if (dist > 3.0517578125e-05f) {          // 2^-15
-    q = rintf(t);
-  } else {
-    const float a = __fmul_rn(127.0f, p);                       // exact
-    const float d = __fmaf_rn(-__fadd_rn(f, 0.5f), m, a);       // sign of 127p - (f+1/2)m
-    if (d > 0.0f) q = f + 1.0f;
-    else if (d < 0.0f) q = f;
-    else q = (fmodf(f, 2.0f) == 0.0f) ? f : f + 1.0f;
-  }
-  q = fminf(fmaxf(q, -128.0f), 127.0f);
-  return (int)q;
-}
-
-// Error-free sum of two fp32 numbers: s + e == a + b exactly (Knuth).
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-
-// (h1 + l1) + (h2 + l2) as a renormalised pair.
-__device__ __forceinline__ void pair_add(float& h1, float& l1, float h2, float l2) {
-  float s, e;
-  two_sum(h1, h2, s, e);
-  e = __fadd_rn(e, __fadd_rn(l1, l2));
-  h1 = __fadd_rn(s, e);
-  l1 = __fsub_rn(e, __fsub_rn(h1, s));
-}
-
-// eight bf16 ones
-__device__ __constant__ uint4 kOnes = {0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u};
 
 // Eight inputs of the gated MLP branch: h = bf16(fl(fl(max(gate, 0)^2) * up)),
 // from fp32 rows [gate (K) | up (K)], packed as bf16 pairs like an input vector.
@@ -188,39 +141,11 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
   __shared__ float2 s_ss[32];
   __shared__ float s_m;
   __shared__ float s_sum;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-    pair_add(hi, lo, h2, l2);
-  }
-  const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;
-  if (lane == 0) { s_max[warp] = amax; s_ss[warp] = make_float2(hi, lo); }
-  __syncthreads();
-  if (warp == 0) {
-    float a = lane < nwarps ? s_max[lane] : 0.0f;
-    float2 p2 = lane < nwarps ? s_ss[lane] : make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-      const float h2 = __shfl_xor_sync(0xffffffffu, p2.x, o), l2 = __shfl_xor_sync(0xffffffffu, p2.y, o);
-      pair_add(p2.x, p2.y, h2, l2);
-    }
-    if (lane == 0) { s_m = a; s_sum = __fadd_rn(p2.x, p2.y); }
-  }
-  __syncthreads();
+  block_stats(amax, hi, lo, tid, T >> 5, s_max, s_ss, &s_m, &s_sum);
 
   const float m = fmaxf(s_m, 1e-8f);
   const float s = __fdiv_rn(127.0f, m);
-  if (tid == 0) {
-    float sigma = __fdiv_rn(m, 127.0f);
-    if (rms_eps >= 0.0f) {
-      const float ms = __fdiv_rn(s_sum, (float)K);
-      const float r = __frsqrt_rn(__fadd_rn(ms, rms_eps));
-      sigma = __fdiv_rn(__fmul_rn(m, r), 127.0f);
-    }
-    act_scale[row] = sigma;
-  }
+  if (tid == 0) act_scale[row] = act_sigma(m, s_sum, K, rms_eps);
 
   uint2* qr = reinterpret_cast<uint2*>(x_q + (size_t)row * K);
   const int64_t Kp = act_ops_kpad(K);

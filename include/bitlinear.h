@@ -260,6 +260,24 @@ bitlinear_status bitlinear_forward(const int8_t *x_q, const float *act_scale, co
  * codes and the per-token scales. */
 size_t bitlinear_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/* Which kernels bitlinear_linear_forward launches for this shape (the results do
+ * not depend on it):
+ *   BITLINEAR_ROUTE_FUSED    one kernel: RMSNorm, quantization and the int8-code
+ *                            contraction together (one token, K <= 8192);
+ *   BITLINEAR_ROUTE_CODES    quantization to int8 codes, then the CUDA-core
+ *                            contraction on them (two tokens with small K, or one
+ *                            token with K > 8192);
+ *   BITLINEAR_ROUTE_DECODE   quantization to the operand form, then the tcgen05
+ *                            decode contraction (up to 32 tokens);
+ *   BITLINEAR_ROUTE_PREFILL  quantization to the operand form, then the tcgen05
+ *                            prefill contraction (more tokens).
+ * -1 for shapes the call rejects. */
+#define BITLINEAR_ROUTE_FUSED 0
+#define BITLINEAR_ROUTE_CODES 1
+#define BITLINEAR_ROUTE_DECODE 2
+#define BITLINEAR_ROUTE_PREFILL 3
+int bitlinear_linear_route(int64_t M, int64_t N, int64_t K);
+
 /*
  * The whole BitLinear layer in one call ([P4-code] BitLinear.forward: RMSNorm,
  * activation_quant, the ternary product and the rescale; [P1-impl]

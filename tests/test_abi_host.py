@@ -49,6 +49,23 @@ def test_codes_route_limit_matches_the_header():
     assert m and int(m.group(1)) == bl.CODES_MAX_M
 
 
+def test_linear_route(L):
+    route = L.bitlinear_linear_route
+    assert route(1, 2560, 2560) == bl.ROUTE_FUSED            # one token, K <= 8192: one kernel
+    assert route(1, 4096, 8192) == bl.ROUTE_FUSED
+    assert route(1, 4096, 14336) == bl.ROUTE_CODES           # one token, longer K: quant + codes kernel
+    assert route(2, 3840, 2560) == bl.ROUTE_CODES
+    assert route(2, 28672, 4096) == bl.ROUTE_DECODE          # two tokens, 56 MiB of weights: tcgen05
+    assert route(2, 2560, 6912) == bl.ROUTE_DECODE           # two tokens, K > 4096
+    assert route(3, 2560, 2560) == bl.ROUTE_DECODE
+    assert route(32, 2560, 2560) == bl.ROUTE_DECODE
+    assert route(33, 2560, 2560) == bl.ROUTE_PREFILL
+    assert route(0, 2560, 2560) == -1 and route(1, 24, 2560) == -1 and route(1, 2560, 100) == -1
+    for name, value in [("FUSED", 0), ("CODES", 1), ("DECODE", 2), ("PREFILL", 3)]:
+        assert re.search(rf"#define BITLINEAR_ROUTE_{name} {value}\b", open(os.path.join(HEADER_DIR, "bitlinear.h")).read())
+        assert getattr(bl, f"ROUTE_{name}") == value
+
+
 def test_status_strings_and_version(L):
     assert L.bitlinear_abi_version() == 1
     for s in range(11):

@@ -146,3 +146,20 @@ def test_linear_residual_and_pdl_chain(M):
     got = res.cpu().float().numpy().astype(np.float64)
     scale = np.maximum(np.abs(r0f), np.abs(o_y2))
     assert np.all(np.abs(got - (r0f + o_y2)) <= 2.0 ** -7 * scale + 1e-30)
+
+
+@pytest.mark.parametrize("K,N,gain,rms", [(128, 144, True, True), (1152, 272, False, True), (2560, 3840, True, True),
+                                          (6912, 2560, True, False), (8192, 400, True, True)])
+def test_linear_one_token_fused(K, N, gain, rms):
+    # one token, K <= 8192: RMSNorm, quantization and the contraction in one kernel.  Its
+    # codes, scale, accumulators and outputs equal the oracle's and, bit for bit, those of
+    # the two-kernel path (quantization, then the contraction on the int8 codes)
+    assert bl.bitlinear_linear_route(1, N, K) == bl.ROUTE_FUSED
+    eps = RMS_EPS if rms else -1.0
+    r = run_linear(1, N, K, torch.float32, seed=K + N, gain=gain, rms_eps=eps, flags=bl.FLAG_PDL)
+    xq2, sc2 = bl.bitlinear_quant_act(r["x"].cuda(), None if r["g"] is None else r["g"].cuda(), eps)
+    acc2 = torch.empty((1, N), dtype=torch.int32, device="cuda")
+    y2 = bl.bitlinear_forward(xq2, sc2, r["packed"], r["w_scale"], out_dtype=torch.float32, acc_debug=acc2)
+    torch.cuda.synchronize()
+    assert torch.equal(r["xq"], xq2) and torch.equal(r["sc"], sc2)
+    assert torch.equal(r["acc"], acc2) and torch.equal(r["y"], y2)
