@@ -1,8 +1,10 @@
 // bitlinear_block_forward: the BitLinear projections of a stack of BitNet
 // b1.58 transformer layers, chained on one stream (contract in bitlinear.h).
 //
-// Per layer eight kernels, each launched as a programmatic dependent of the
-// previous one (its weight copies start before the previous kernel ends):
+// Per layer eight kernels (five for one token, where the QKV, O and gate+up
+// layers each run as one kernel that also quantizes), each launched as a
+// programmatic dependent of the previous one (its weights are read before the
+// previous kernel ends):
 //   quant(x, g_qkv) -> forward(qkv, bf16) -> quant(qkv[:, :H], g_o)
 //   -> forward(o, bf16 residual add into x) -> quant(x, g_gate_up)
 //   -> forward(gate_up, fp32) -> quant(ReLU^2-gated h, g_down)
@@ -101,14 +103,26 @@ extern "C" bitlinear_status bitlinear_block_forward(const bitlinear_layer* layer
       e = launch_forward(codes ? codes_buf : nullptr, w.scale, codes ? nullptr : w.ops, packed, wscale, M, N, K,
                          out_dtype, y, nullptr, nullptr, err, true, s);
   };
+  // one projection on bf16 rows `in` (pitch ld): for one token one kernel (RMSNorm,
+  // quantization and contraction together), else quantization, then the contraction
+  auto layer = [&](const uint16_t* in, int64_t ld, const void* gain, const uint8_t* packed, const float* wscale,
+                   int64_t N, int64_t K, int out_dtype, void* y) {
+    if (fused_route(M, N, K)) {
+      if (e == cudaSuccess)
+        e = launch_linear_dp4a(in, static_cast<const uint16_t*>(gain), rms_eps, packed, wscale, N, K, out_dtype, y,
+                               nullptr, nullptr, nullptr, pdl, s);
+      pdl = true;
+      return;
+    }
+    quant(in, ld, nullptr, gain, N, K);
+    forward(packed, wscale, N, K, out_dtype, y);
+  };
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const bitlinear_layer& L = layers[l];
-    quant(x, H, nullptr, L.gain_qkv, NQKV, H);
-    forward(L.qkv, L.qkv_scale, NQKV, H, BITLINEAR_OUT_BF16, w.qkv);
-    quant(w.qkv, NQKV, nullptr, L.gain_o, H, H);                  // the query slice stands in for attention
-    forward(L.o, L.o_scale, H, H, BITLINEAR_OUT_BF16_ADD, x_bf16);
-    quant(x, H, nullptr, L.gain_gate_up, 2 * F, H);
-    forward(L.gate_up, L.gate_up_scale, 2 * F, H, BITLINEAR_OUT_F32, w.gu);
+    layer(x, H, L.gain_qkv, L.qkv, L.qkv_scale, NQKV, H, BITLINEAR_OUT_BF16, w.qkv);
+    // the query slice stands in for attention
+    layer(w.qkv, NQKV, L.gain_o, L.o, L.o_scale, H, H, BITLINEAR_OUT_BF16_ADD, x_bf16);
+    layer(x, H, L.gain_gate_up, L.gate_up, L.gate_up_scale, 2 * F, H, BITLINEAR_OUT_F32, w.gu);
     quant(nullptr, F, w.gu, L.gain_down, H, F);                   // h = bf16(relu(gate)^2 * up)
     forward(L.down, L.down_scale, H, F, BITLINEAR_OUT_BF16_ADD, x_bf16);
   }
