@@ -1,11 +1,15 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
 same seeded inputs.
 
-Bars (derivations in DESIGN.md, "Tolerances"):
+Bars:
 * int8 codes, packed bytes, gamma and int32 accumulators: bit-exact;
-* act_scale (sigma): relative error <= 5e-7 against the oracle's fp64 value;
-* fp32 output: relative error <= 1e-6 against the oracle's fp64 output;
-* bf16 output: within 1 bf16 ulp of the oracle's fp64 output rounded to bf16.
+* act_scale (sigma): relative error <= 5e-7 against the oracle's fp64 value (the
+  GPU sums x^2 as an error-free fp32 pair, then takes five IEEE-rounded steps:
+  at most 4.5 * 2^-24 = 2.7e-7);
+* fp32 output: relative error <= 1e-6 against the oracle's fp64 output (sigma's
+  error plus two fp32 roundings: at most 3.9e-7);
+* bf16 output: within 1 bf16 ulp of the oracle's fp64 output rounded to bf16 (the
+  fp32 value is that close to the exact one).
 """
 import numpy as np
 import pytest
