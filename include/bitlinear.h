@@ -281,16 +281,19 @@ int bitlinear_linear_route(int64_t M, int64_t N, int64_t K);
 /*
  * The whole BitLinear layer in one call ([P4-code] BitLinear.forward: RMSNorm,
  * activation_quant, the ternary product and the rescale; [P1-impl]
- * bitlinear_forward(x, W_packed, s)): enqueues bitlinear_quant_act into the
- * workspace, then bitlinear_forward on its operand form, the second launch
- * overlapping the first (programmatic dependent launch).  Results equal those of
- * the two calls.
+ * bitlinear_forward(x, W_packed, s)).  For one token with K <= 8192 a single
+ * kernel does all of it (BITLINEAR_ROUTE_FUSED); otherwise the call enqueues
+ * bitlinear_quant_act into the workspace (int8 codes or the operand form), then
+ * bitlinear_forward on it, the second launch overlapping the first (programmatic
+ * dependent launch).  bitlinear_linear_route tells which.  Results equal those of
+ * the two calls bit for bit.
  *
  * x_bf16, gain_bf16, rms_eps  as bitlinear_quant_act (K % 128 == 0 here).
  * packed, w_scale, M, N, K, out_dtype, y, acc_debug  as bitlinear_forward.
  * x_q       [M,K] int8 out, or NULL.  act_scale [M] fp32 out, or NULL (then kept
  *           in the workspace).
- * workspace >= bitlinear_linear_workspace_bytes(M,N,K) bytes of device scratch.
+ * workspace >= bitlinear_linear_workspace_bytes(M,N,K) bytes of device scratch
+ *           (required on every route; the one-kernel route leaves it untouched).
  *           Contents on entry do not matter.
  * flags     0 or BITLINEAR_FLAG_PDL (the first launch may overlap the work
  *           already on the stream).
