@@ -49,6 +49,15 @@ def test_codes_route_limit_matches_the_header():
     assert m and int(m.group(1)) == bl.CODES_MAX_M
 
 
+def test_codes_route_needs_no_workspace(L):
+    # bitlinear_forward given x_q: no scratch where the int8-code kernel takes it
+    ws = L.bitlinear_forward_workspace_bytes
+    assert ws(1, 2560, 2560) == 0 and ws(1, 4096, 65536) == 0 and ws(2, 3840, 2560) == 0
+    assert ws(2, 28672, 4096) == L.bitlinear_act_ops_bytes(2, 4096)     # 56 MiB of weights: tcgen05
+    assert ws(3, 2560, 2560) == L.bitlinear_act_ops_bytes(3, 2560)
+    assert ws(64, 2560, 2560) == L.bitlinear_act_ops_bytes(64, 2560)
+
+
 def test_linear_route(L):
     route = L.bitlinear_linear_route
     assert route(1, 2560, 2560) == bl.ROUTE_FUSED            # one token, K <= 8192: one kernel
