@@ -142,3 +142,73 @@ def test_tensor_core_operand_split_is_exact():
     # times K <= 65536 ternary weights, at most 2^19; the decode kernel adds 16 h-sums and
     # the l-sums in int32, and the prefill kernel's single accumulator is bounded by 127 K
     assert 8 * 65536 <= 2 ** 24 and 127 * 65536 <= 2 ** 24
+
+
+# ---- the one-token layer kernel's statistics equal the quantization kernel's --------
+# Both reduce (max|x g|, sum x^2 as an fp32 pair) with the same per-thread order and
+# xor trees; the layer kernel only has more warps, whose partials are zero.  Restated
+# in float32 numpy (IEEE round to nearest even, like the GPU's __fadd_rn and friends).
+
+F32 = np.float32
+
+
+def _two_sum(a, b):
+    s = F32(a + b)
+    bb = F32(s - a)
+    return s, F32(F32(a - F32(s - bb)) + F32(b - bb))
+
+
+def _pair_add(h1, l1, h2, l2):
+    s, e = _two_sum(h1, h2)
+    e = F32(e + F32(l1 + l2))
+    h = F32(s + e)
+    return h, F32(e - F32(h - s))
+
+
+def _xor_tree(vals):
+    """vals: 32 lanes of (amax, hi, lo); returns lane 0 after offsets 16, 8, 4, 2, 1."""
+    v = list(vals)
+    for o in (16, 8, 4, 2, 1):
+        nv = []
+        for i in range(32):
+            a1, h1, l1 = v[i]
+            a2, h2, l2 = v[i ^ o]
+            h, l = _pair_add(h1, l1, h2, l2)
+            nv.append((max(a1, a2), h, l))
+        v = nv
+    return v[0]
+
+
+def _row_stats(x, g, T):
+    U = len(x) // 16
+    per = []
+    for t in range(T):
+        a, hi, lo = F32(0), F32(0), F32(0)
+        if t < U:
+            for j in range(16):
+                xv, gv = x[16 * t + j], g[16 * t + j]
+                a = max(a, abs(F32(xv * gv)))
+                s, e = _two_sum(hi, F32(xv * xv))
+                hi, lo = s, F32(lo + e)
+        per.append((a, hi, lo))
+    warps = [_xor_tree(per[32 * w:32 * w + 32]) for w in range(T // 32)]
+    lanes = [warps[i] if i < len(warps) else (F32(0), F32(0), F32(0)) for i in range(32)]
+    a, h, l = _xor_tree(lanes)
+    return a, F32(h + l)
+
+
+@pytest.mark.parametrize("K", [128, 1152, 2560, 6912])
+def test_layer_kernel_statistics_equal_the_quantization_kernels(K):
+    rng = np.random.default_rng(K)
+    # bf16-valued inputs and gains (8 significant bits), wide exponent range
+    x = (rng.standard_normal(K) * np.exp2(rng.integers(-6, 7, K))).astype(np.float32)
+    x = (x.view(np.uint32) & 0xFFFF0000).view(np.float32)
+    g = (rng.uniform(0.5, 1.5, K).astype(np.float32).view(np.uint32) & 0xFFFF0000).view(np.float32)
+    tq = (K // 16 + 31) // 32 * 32            # the quantization kernel's threads for one row
+    tf = (tq + 127) // 128 * 128              # the layer kernel's
+    a1, s1 = _row_stats(x, g, tq)
+    a2, s2 = _row_stats(x, g, tf)
+    assert a1 == a2 and s1.view(np.uint32) == s2.view(np.uint32)
+    # and the pair sum is the exact sum of squares rounded once, for these inputs
+    exact = sum(int(v) for v in (x.astype(np.float64) ** 2 * 2.0 ** 300).astype(object))
+    assert abs(float(s1) - float(np.float64(exact) * 2.0 ** -300)) <= np.spacing(s1)
