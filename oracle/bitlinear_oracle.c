@@ -175,45 +175,76 @@ static double bf16_to_double(uint16_t h)
 /*
  * [P4-code] BitLinear.forward steps 1-2 and [P4-eq] item 2, per token row t:
  *   RMSNorm:   n_k = x_k * r * g_k,  r = 1 / sqrt(mean_k(x_k^2) + rms_eps)
- *   absmax:    x_q[k] = Clip(Round(n_k * Q_b / max_k|n_k|), -128, 127), Q_b = 127
- *   scale:     sigma = max_k|n_k| / Q_b   (the activation half of the dequant
- *              scale gamma * max|x| / Q_b of item 4)
+ *   absmax:    x_q[k] = Clip(Round(n_k * Q_b / c), -128, 127), Q_b = 127,
+ *              c = max(max_k|n_k|, 1e-8)   (activation_quant clamps the max of
+ *              its input, the normalized row, at 1e-8)
+ *   scale:     sigma = c / Q_b   (the activation half of the dequant scale
+ *              gamma * max|x| / Q_b of item 4)
  *
- * r > 0 is one number per row, so it cancels exactly from n_k / max|n|; the
- * integer codes are therefore those of p_k = x_k * g_k, which is exact in
- * binary64 (two 8-bit significands).  127 * p_k is exact too, and the binary64
- * quotient 127 p / m can never round onto a half-integer that the exact
- * quotient is not, so rint() below returns the exactly rounded code (ties to
- * even).  A row with max|p| below 1e-8 (binary32) is guarded by clamping the
- * max to 1e-8, as activation_quant clamps its scale; an all-zero row gives
- * zero codes.  gain == NULL means g_k = 1; rms_eps < 0 means no RMSNorm
- * (r = 1).  sigma is computed in binary64.
+ * Which side of the clamp a row falls on is decided in binary32, the precision
+ * of the page's code: r32 = fl(1 / fl(sqrt(fl(fl(mean x^2) + rms_eps)))) and
+ * max|n| = fl(max|p| * r32), with p_k = x_k * g_k (exact in binary32: two 8-bit
+ * significands).
+ *
+ * Rows with max|n| >= 1e-8 (every row of real activations): r > 0 is one
+ * number per row, so it cancels exactly from n_k / max|n|, and the integer
+ * codes are those of p_k = x_k * g_k.  127 * p_k is exact in binary64, and the
+ * binary64 quotient 127 p / m (m = max|p|) can never round onto a
+ * half-integer that the exact quotient is not, so rint() below returns the
+ * exactly rounded code (ties to even).  sigma = m * r / 127 in binary64.
+ *
+ * Rows with max|n| < 1e-8 (all-zero rows, rows of tiny values, zero gains):
+ * c = 1e-8 and the codes depend on r; they are formed as the page's code forms
+ * x_norm * (Q_b / c), in binary32: q = rint(fl(fl(p * r32) * fl(127 / 1e-8))).
+ * sigma = 1e-8 / 127.
+ *
+ * gain == NULL means g_k = 1; rms_eps < 0 means no RMSNorm (r = r32 = 1).
  */
 void oracle_act_quant(const uint16_t *x, const uint16_t *gain, double rms_eps,
                       int64_t M, int64_t K, int8_t *xq, double *sigma)
 {
-    const double tiny = (double)1e-8f;
+    const float clampv = 1e-8f;
     int64_t t, k;
     for (t = 0; t < M; ++t) {
         const uint16_t *row = x + t * K;
-        double m = 0.0, ss = 0.0, m_eff, r;
+        double m = 0.0, ss = 0.0;
+        float r32 = 1.0f, nmax;
         for (k = 0; k < K; ++k) {
             double xv = bf16_to_double(row[k]);
             double p = gain ? xv * bf16_to_double(gain[k]) : xv;
             if (fabs(p) > m) m = fabs(p);
             ss += xv * xv;
         }
-        m_eff = m > tiny ? m : tiny;
-        for (k = 0; k < K; ++k) {
-            double xv = bf16_to_double(row[k]);
-            double p = gain ? xv * bf16_to_double(gain[k]) : xv;
-            double v = rint(127.0 * p / m_eff);
-            if (v > 127.0) v = 127.0;
-            if (v < -128.0) v = -128.0;
-            xq[t * K + k] = (int8_t)v;
+        if (rms_eps >= 0.0) {
+            float ms = (float)(ss / (double)K);
+            float v = ms + (float)rms_eps;
+            r32 = 1.0f / sqrtf(v);
         }
-        r = rms_eps >= 0.0 ? 1.0 / sqrt(ss / (double)K + rms_eps) : 1.0;
-        sigma[t] = m_eff * r / 127.0;
+        nmax = (float)m * r32;                 /* m is a binary32 value */
+        if (nmax >= clampv) {
+            double r = rms_eps >= 0.0 ? 1.0 / sqrt(ss / (double)K + rms_eps) : 1.0;
+            for (k = 0; k < K; ++k) {
+                double xv = bf16_to_double(row[k]);
+                double p = gain ? xv * bf16_to_double(gain[k]) : xv;
+                double v = rint(127.0 * p / m);
+                if (v > 127.0) v = 127.0;
+                if (v < -128.0) v = -128.0;
+                xq[t * K + k] = (int8_t)v;
+            }
+            sigma[t] = m * r / 127.0;
+        } else {
+            const float sc = 127.0f / clampv;
+            for (k = 0; k < K; ++k) {
+                float xv = (float)bf16_to_double(row[k]);
+                float p = gain ? xv * (float)bf16_to_double(gain[k]) : xv;
+                float n = p * r32;
+                float v = rintf(n * sc);
+                if (v > 127.0f) v = 127.0f;
+                if (v < -128.0f) v = -128.0f;
+                xq[t * K + k] = (int8_t)v;
+            }
+            sigma[t] = (double)clampv / 127.0;
+        }
     }
 }
 

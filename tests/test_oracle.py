@@ -226,13 +226,46 @@ def test_act_quant_gain_rmsnorm_worked_example():
 
 
 def _exact_codes(xb, gb):
-    """Brute force with exact rationals: Round_half_even(127 * p / max|p|), p = x*g."""
+    """Brute force with exact rationals: Round_half_even(127 * p / max|p|), p = x*g.
+
+    This is the definition for rows whose normalized max|n| = max|p| * r is not
+    clamped (r <= 1/sqrt(eps) < 317, so max|p| >= 2^-20 keeps max|n| far above 1e-8
+    whenever the row has no tiny values beside it); the callers stay in that range."""
     x = [Fraction(float(v)) for v in bf16_bits_to_f64(xb)]
     g = [Fraction(float(v)) for v in bf16_bits_to_f64(gb)] if gb is not None else [1] * len(x)
     p = [a * b for a, b in zip(x, g)]
     m = max(abs(v) for v in p)
-    m = max(m, Fraction(float(np.float32(1e-8))))
+    assert m >= Fraction(1, 2**20)
     return [max(-128, min(127, round(127 * v / m))) for v in p]
+
+
+@pytest.mark.parametrize("key", ["act_clamp_regular_tiny_row", "act_clamp_plain_tiny_row",
+                                 "act_clamp_small_rmsnorm_row"])
+def test_act_quant_clamp_worked_examples(key):
+    # activation_quant clamps the max of the RMSNorm output, not of the raw row
+    ex = GOLDEN[key]
+    xb = bf16([ex["x"]])
+    assert (bf16_bits_to_f64(xb)[0] == np.array(ex["x"])).all()
+    xq, sigma = act_quant(xb, None, float(np.float32(ex["rms_eps"])) if ex["rms_eps"] >= 0 else -1.0)
+    assert xq[0].tolist() == ex["x_q"]
+    if "sigma_den" in ex:
+        assert sigma[0] == float(np.float32(1e-8)) / ex["sigma_den"]
+
+
+def test_act_quant_zero_row_takes_the_clamp():
+    # an all-zero row: zero codes and the clamped scale 1e-8 / 127, with or without RMSNorm
+    z = np.zeros((2, 64), dtype=np.uint16)
+    for eps in (RMS_EPS, -1.0):
+        zq, zs = act_quant(z, None, eps)
+        assert (zq == 0).all() and (zs == float(np.float32(1e-8)) / 127.0).all()
+
+
+def test_f32_to_bf16_bits_golden():
+    ex = GOLDEN["bf16_round_nearest_even"]
+    src = np.array([int(a, 16) for a, _, _ in ex["cases"]], dtype=np.uint32).view(np.float32)
+    want = [int(b, 16) for _, b, _ in ex["cases"]]
+    got = f32_to_bf16_bits(src).tolist()
+    assert got == want, [(c[2], hex(g)) for c, g in zip(ex["cases"], got) if int(c[1], 16) != g]
 
 
 def test_act_quant_matches_exact_rational_bruteforce():
