@@ -14,10 +14,15 @@
 //
 // sigma = max|x*g| * r / 127 with r = 1/sqrt(sum/K + eps): every step is one
 // IEEE round-to-nearest operation, so with u = 2^-24 the result is within
-// 4.5 u (2.7e-7) of the exact value: sum u, /K 2u, +eps 3u, rsqrt 2.5u,
-// *m 3.5u, /127 4.5u.
+// 3.5 u (2.1e-7) of the exact value: sum u, /K 2u, +eps 3u, sqrt 2u, 1/ 2.5u,
+// *m 3u, /127 3.5u.
 //
-// Codes.  r > 0 is one number per row, so Round(127 n/max|n|) with n = x*r*g
+// Clamp (activation_quant clamps max|x_norm| at 1e-8): a row whose max|n|,
+// formed as fl(max|x*g| * r), is below 1e-8 takes 1e-8 as its max; its codes
+// are rint(fl(fl(p * r) * fl(127 / 1e-8))) and sigma = fl(1e-8 / 127)
+// (quant_math.cuh, row_quant).  Only rows of zeros or of tiny values reach it.
+//
+// Codes of the other rows.  r > 0 is one number per row, so Round(127 n/max|n|) with n = x*r*g
 // equals Round(127 p/max|p|) with p = x*g, and p is exact in fp32 (two 8-bit
 // significands).  The kernel forms t = p * fl(127/m) (relative error <= 2^-23,
 // i.e. |t - 127p/m| < 1.6e-5) and takes rint(t) unless t lies within 2^-15 of
@@ -69,7 +74,7 @@ __global__ void __launch_bounds__(1024)
 quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restrict__ glu,
                  const uint4* __restrict__ gain, float rms_eps,
                  int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale,
-                 uint8_t* __restrict__ x_ops, int64_t M) {
+                 uint8_t* __restrict__ x_ops, int64_t M, const uint8_t* pf, uint64_t pf_bytes) {
   const int V = K >> 3;                      // 16-byte vectors per row
   const int U = (V + 1) >> 1;                // units of 16 inputs
   const int row = blockIdx.x;
@@ -100,6 +105,9 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
       if (u < U && (u & 3) == 0) prefetch_l2(xr + 2 * u);   // one per 128-byte line
     }
   }
+  // the caller's L2 prefetch (the weights of the contraction that follows), spread
+  // over the first warp
+  if (tid < 32) l2_prefetch_share(pf, pf_bytes, tid, 32);
   // Let the next kernel launch now: it waits for this one to complete, and this one
   // completes only after the kernel before it (the wait below), so the next kernel
   // can set up and prefetch its weights while the previous one still runs.
@@ -143,9 +151,8 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
   __shared__ float s_sum;
   block_stats(amax, hi, lo, tid, T >> 5, s_max, s_ss, &s_m, &s_sum);
 
-  const float m = fmaxf(s_m, 1e-8f);
-  const float s = __fdiv_rn(127.0f, m);
-  if (tid == 0) act_scale[row] = act_sigma(m, s_sum, K, rms_eps);
+  const RowQuant rq = row_quant(s_m, s_sum, K, rms_eps);
+  if (tid == 0) act_scale[row] = rq.sigma;
 
   uint2* qr = reinterpret_cast<uint2*>(x_q + (size_t)row * K);
   const int64_t Kp = act_ops_kpad(K);
@@ -162,7 +169,7 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
         if constexpr (kPreGain) unpack8(gv_[i][hv], gf);
         else unpack8((gain && v < V) ? __ldg(gain + v) : kOnes, gf);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) q[8 * hv + j] = quant_code(__fmul_rn(xf[j], gf[j]), s, m);
+        for (int j = 0; j < 8; ++j) q[8 * hv + j] = row_code(__fmul_rn(xf[j], gf[j]), rq);
         if (v < V && x_q) {
           uint32_t w0 = 0, w1 = 0;
 #pragma unroll
@@ -195,7 +202,7 @@ constexpr uint32_t kRowsSpin = 1u << 24;
 __global__ void __launch_bounds__(kRowsThreads, 2)
 quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __restrict__ gain, float rms_eps,
                   int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale, uint8_t* __restrict__ x_ops,
-                  int64_t M, int* dev_err) {
+                  int64_t M, int* dev_err, const uint8_t* pf, uint64_t pf_bytes) {
   extern __shared__ __align__(16) uint8_t qsm[];
   const int rb = K * 2;                            // bytes of a row (a multiple of 16)
   const uint32_t buf0 = smem_u32(qsm), gbuf = buf0 + 2 * rb;
@@ -217,6 +224,7 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __
   for (int v = tid; v < V; v += kRowsThreads)
     *reinterpret_cast<uint4*>(qsm + 2 * rb + 16 * v) =
         gain ? __ldg(reinterpret_cast<const uint4*>(gain) + v) : kOnes;
+  if (tid < 32) l2_prefetch_share(pf, pf_bytes, tid, 32);
   __syncthreads();
   pdl_launch_dependents();                         // as in quant_act_kernel
   pdl_wait();                                      // x may be the previous kernel's output
@@ -297,17 +305,8 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __
       }
     }
     __syncthreads();
-    const float m = fmaxf(s_m, 1e-8f);
-    const float sc = __fdiv_rn(127.0f, m);
-    if (tid == 0) {
-      float sigma = __fdiv_rn(m, 127.0f);
-      if (rms_eps >= 0.0f) {
-        const float ms = __fdiv_rn(s_sum, (float)K);
-        const float r = __frsqrt_rn(__fadd_rn(ms, rms_eps));
-        sigma = __fdiv_rn(__fmul_rn(m, r), 127.0f);
-      }
-      act_scale[row] = sigma;
-    }
+    const RowQuant rq = row_quant(s_m, s_sum, K, rms_eps);
+    if (tid == 0) act_scale[row] = rq.sigma;
     // pass 2: codes, the int8 row and the operand form
     uint2* qr = x_q ? reinterpret_cast<uint2*>(x_q + row * K) : nullptr;
     for (int u = tid; u < (int)(Kp >> 4); u += kRowsThreads) {
@@ -320,7 +319,7 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __
           unpack8(lds128(xb + 16 * v), xf);
           unpack8(lds128(gbuf + 16 * v), gf);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) q[8 * hv + j] = quant_code(__fmul_rn(xf[j], gf[j]), sc, m);
+          for (int j = 0; j < 8; ++j) q[8 * hv + j] = row_code(__fmul_rn(xf[j], gf[j]), rq);
           if (qr) {
             uint32_t w0 = 0, w1 = 0;
 #pragma unroll
@@ -348,13 +347,13 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __
 
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,
                              int64_t K, int8_t* x_q, float* act_scale, uint8_t* x_ops, bool pdl,
-                             cudaStream_t stream) {
-  return launch_quant_act_ex(x, K, nullptr, gain, rms_eps, M, K, x_q, act_scale, x_ops, pdl, stream);
+                             cudaStream_t stream, L2Prefetch pf) {
+  return launch_quant_act_ex(x, K, nullptr, gain, rms_eps, M, K, x_q, act_scale, x_ops, pdl, stream, pf);
 }
 
 cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu, const uint16_t* gain,
                                 float rms_eps, int64_t M, int64_t K, int8_t* x_q, float* act_scale,
-                                uint8_t* x_ops, bool pdl, cudaStream_t stream) {
+                                uint8_t* x_ops, bool pdl, cudaStream_t stream, L2Prefetch pf) {
   if (M == 0) return cudaSuccess;
   const int sms = num_sms();
   // Many long rows of bf16 input: persistent CTAs that stream rows through shared
@@ -382,7 +381,7 @@ cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu,
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     cudaError_t e = cudaLaunchKernelEx(&cfg, quant_rows_kernel, x, ld, gain, rms_eps, (int)K, x_q, act_scale,
-                                       x_ops, M, dev_err);
+                                       x_ops, M, dev_err, pf.p, pf.bytes);
     count_launches(1);
     return e;
   }
@@ -415,10 +414,10 @@ cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu,
   const uint4* gv = reinterpret_cast<const uint4*>(gain);
   cudaError_t e;
   switch (tv) {
-    case 1: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<1>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
-    case 2: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
-    case 4: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<4>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
-    default: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<8>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    case 1: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<1>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M, pf.p, pf.bytes); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M, pf.p, pf.bytes); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<4>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M, pf.p, pf.bytes); break;
+    default: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<8>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M, pf.p, pf.bytes); break;
   }
   count_launches(1);
   return e;

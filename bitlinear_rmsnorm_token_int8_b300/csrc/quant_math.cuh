@@ -86,12 +86,46 @@ __device__ __forceinline__ void block_stats(float amax, float hi, float lo, int 
   __syncthreads();
 }
 
-// sigma = max|x g| * r / 127 with r = 1/sqrt(sum/K + eps), or max|x g| / 127 without RMSNorm.
-__device__ __forceinline__ float act_sigma(float m, float sum, int K, float rms_eps) {
-  if (rms_eps < 0.0f) return __fdiv_rn(m, 127.0f);
-  const float ms = __fdiv_rn(sum, (float)K);
-  const float r = __frsqrt_rn(__fadd_rn(ms, rms_eps));
-  return __fdiv_rn(__fmul_rn(m, r), 127.0f);
+// activation_quant's clamp of the normalized row's max|n|, n = x r g
+constexpr float kActClamp = 1e-8f;
+
+// The per-row constants of the quantization, formed identically by every
+// thread from the row's max|x g| (m, exact) and fl32 sum of x^2.
+//   r     = fl(1 / fl(sqrt(fl(fl(sum / K) + eps))))   (1 without RMSNorm)
+//   max|n| = fl(m r); a row with max|n| >= 1e-8 quantizes on p = x g with
+//   s = fl(127 / m) (r cancels from n / max|n|) and sigma = fl(max|n| / 127);
+//   a row below the clamp ("small") has c = 1e-8: codes rint(fl(fl(p r) fl(127 / c)))
+//   and sigma = fl(c / 127).
+struct RowQuant {
+  float m;       // max|p| (regular rows)
+  float s;       // fl(127 / m), or fl(127 / c) for small rows
+  float r;       // RMSNorm factor (used by small rows' codes)
+  float sigma;   // dequantization factor of the row
+  bool small;    // max|n| < 1e-8: the clamp applies
+};
+
+__device__ __forceinline__ RowQuant row_quant(float m, float sum, int K, float rms_eps) {
+  RowQuant q;
+  q.r = 1.0f;
+  if (rms_eps >= 0.0f) q.r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, (float)K), rms_eps)));
+  const float nmax = __fmul_rn(m, q.r);
+  q.small = !(nmax >= kActClamp);
+  q.m = m;
+  if (!q.small) {
+    q.s = __fdiv_rn(127.0f, m);
+    q.sigma = __fdiv_rn(nmax, 127.0f);
+  } else {
+    q.s = __fdiv_rn(127.0f, kActClamp);
+    q.sigma = __fdiv_rn(kActClamp, 127.0f);
+  }
+  return q;
+}
+
+// Code of input p = x g of a row with constants q.
+__device__ __forceinline__ int row_code(float p, const RowQuant& q) {
+  if (!q.small) return quant_code(p, q.s, q.m);
+  const float t = __fmul_rn(__fmul_rn(p, q.r), q.s);
+  return (int)fminf(fmaxf(rintf(t), -128.0f), 127.0f);
 }
 
 }  // namespace bitlinear

@@ -23,7 +23,9 @@ and the composition of the steps.  Each function names the passage it follows:
             Transformer Block" (q/k/v/o and gate/up/down projections, residual
             adds around the attention and the FFN).
 
-Parity pins: every function here is pinned by ``tests/test_oracle.py``;
+Parity pins: every function here is pinned by ``tests/test_oracle.py`` (hand-worked
+values in ``tests/golden/worked_examples.json``, including the bf16 rounding of
+``f32_to_bf16_bits`` and the clamp of tiny rows);
 ``block_layer`` is pinned only by identities (zero projections leave the
 residual stream unchanged, the gate's closed form) and by a recomputation
 with dense fp64 matmuls, its attention stand-in being a reading, not a
@@ -201,6 +203,9 @@ def act_quant(x_bits: np.ndarray, gain_bits: np.ndarray | None, rms_eps: float):
 
     x_bits: [M,K] uint16 bf16 patterns; gain_bits: [K] uint16 or None;
     rms_eps < 0 disables RMSNorm.  Returns (x_q int8 [M,K], sigma float64 [M]).
+    As activation_quant, the max of the normalized row is clamped at 1e-8: rows
+    below it (zeros, tiny values) take 1e-8 as their max, and their codes are
+    formed from x * r * g in binary32 (see bitlinear_oracle.c).
     """
     lib = _load()
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)

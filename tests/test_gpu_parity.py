@@ -11,6 +11,9 @@ Bars:
 * bf16 output: within 1 bf16 ulp of the oracle's fp64 output rounded to bf16 (the
   fp32 value is that close to the exact one).
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -124,6 +127,44 @@ def test_quant_act_edge_rows():
         assert (xq == oq).all()
         assert np.all(np.abs(sc - osig) <= SIGMA_RTOL * osig)
     assert (xq[0] == 0).all()
+
+
+_GOLDEN = json.load(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_examples.json")))
+
+
+@pytest.mark.parametrize("key", ["act_clamp_regular_tiny_row", "act_clamp_plain_tiny_row",
+                                 "act_clamp_small_rmsnorm_row"])
+@pytest.mark.parametrize("kernel", ["one_row_per_cta", "many_rows", "one_token_layer"])
+def test_quant_clamp_golden_rows_every_kernel(key, kernel):
+    # activation_quant clamps the max of the RMSNorm output at 1e-8: the hand-worked rows
+    # (zero-padded, which changes neither max|n| nor the rounding of mean(x^2) + eps)
+    # through each kernel that quantizes
+    ex = _GOLDEN[key]
+    eps = RMS_EPS if ex["rms_eps"] >= 0 else -1.0
+    K = 4104 if kernel == "many_rows" else 512
+    M = 600 if kernel == "many_rows" else 1
+    rows = np.zeros((M, K), dtype=np.float32)
+    rows[:, :8] = ex["x"]
+    bits = oracle.f32_to_bf16_bits(rows)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    want = np.zeros((M, K), dtype=np.int8)
+    want[:, :8] = ex["x_q"]
+    if kernel == "one_token_layer":
+        N = 128
+        assert bl.bitlinear_linear_route(1, N, K) == bl.ROUTE_FUSED
+        packed, w_scale, _ = bl.bitlinear_pack_weights(synth.latent_weights(N, K, seed=5).cuda())
+        xq = torch.empty((1, K), dtype=torch.int8, device="cuda")
+        sc = torch.empty(4, dtype=torch.float32, device="cuda")[:1]
+        bl.bitlinear_linear_forward(x.cuda(), None, eps, packed, w_scale, out_dtype=torch.float32, x_q=xq,
+                                    act_scale=sc)
+        torch.cuda.synchronize()
+        xq, sc = xq.cpu().numpy(), sc.cpu().numpy().astype(np.float64)
+    else:
+        xq, sc = gpu_quant(x, None, eps)
+    oq, osig = oracle.act_quant(bits, None, eps)
+    assert (oq == want).all()
+    assert (xq == want).all()
+    assert np.all(np.abs(sc - osig) <= SIGMA_RTOL * osig)
 
 
 def test_quant_act_empty_is_noop():
