@@ -30,7 +30,7 @@ __all__ = [
     "STATUS", "bitlinear_kernel_launches", "bitlinear_act_ops_bytes", "FLAG_PDL", "OUT_BF16_ADD",
     "bitlinear_block_forward", "bitlinear_block_workspace_bytes", "pack_stacked", "LAYER_FIELDS",
     "bitlinear_linear_forward", "bitlinear_linear_workspace_bytes", "CODES_MAX_M", "bitlinear_linear_route",
-    "ROUTE_FUSED", "ROUTE_CODES", "ROUTE_DECODE", "ROUTE_PREFILL",
+    "ROUTE_FUSED", "ROUTE_CODES", "ROUTE_DECODE", "ROUTE_PREFILL", "bitlinear_prefill_cluster_size",
 ]
 
 OUT_F32 = 0
@@ -82,7 +82,7 @@ def lib() -> ctypes.CDLL:
         L.bitlinear_quant_act.restype = I
         L.bitlinear_forward_workspace_bytes.argtypes = [I64, I64, I64]
         L.bitlinear_forward_workspace_bytes.restype = SZ
-        L.bitlinear_forward.argtypes = [P, P, P, P, P, I64, I64, I64, I, P, P, P, SZ, U, P]
+        L.bitlinear_forward.argtypes = [P, P, P, P, P, I64, I64, I64, I, P, P, P, SZ, P, SZ, U, P]
         L.bitlinear_forward.restype = I
         L.bitlinear_get_device_error.argtypes = [P]
         L.bitlinear_get_device_error.restype = I
@@ -94,7 +94,9 @@ def lib() -> ctypes.CDLL:
         L.bitlinear_linear_workspace_bytes.restype = SZ
         L.bitlinear_linear_route.argtypes = [I64, I64, I64]
         L.bitlinear_linear_route.restype = I
-        L.bitlinear_linear_forward.argtypes = [P, P, F, P, P, I64, I64, I64, I, P, P, P, P, P, SZ, U, P]
+        L.bitlinear_prefill_cluster_size.argtypes = [P, I64, I64, I64]
+        L.bitlinear_prefill_cluster_size.restype = I
+        L.bitlinear_linear_forward.argtypes = [P, P, F, P, P, I64, I64, I64, I, P, P, P, P, P, SZ, P, SZ, U, P]
         L.bitlinear_linear_forward.restype = I
         _lib = L
     return _lib
@@ -112,6 +114,17 @@ def _ptr(t):
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _prefetch(prefetch):
+    """(address, bytes) of an L2 prefetch hint: None, a CUDA tensor (all of it) or a
+    (tensor, bytes) pair."""
+    if prefetch is None:
+        return None, 0
+    t, n = prefetch if isinstance(prefetch, tuple) else (prefetch, None)
+    _cuda(t, "prefetch")
+    total = t.numel() * t.element_size()
+    return ctypes.c_void_p(t.data_ptr()), total if n is None else min(int(n), total)
 
 
 def _cuda(t: torch.Tensor, name: str, dtype=None):
@@ -197,11 +210,13 @@ def bitlinear_quant_act(x: torch.Tensor, gain=None, rms_eps: float = 1e-5, x_q=N
 
 def bitlinear_forward(x_q, act_scale: torch.Tensor, packed: torch.Tensor,
                       w_scale: torch.Tensor, out_dtype=torch.bfloat16, y=None, acc_debug=None,
-                      workspace=None, x_ops=None, flags: int = 0, K: int | None = None, stream=None):
+                      workspace=None, x_ops=None, flags: int = 0, K: int | None = None, stream=None,
+                      prefetch=None):
     """y [M,N] = dequant(x_q . W_q^T) (CUDA).  ``acc_debug``: optional int32 [M,N] out.
 
     N is ``w_scale``'s length.  ``x_ops`` (from :func:`bitlinear_quant_act`) skips the
-    conversion of x_q; x_q may then be None, and ``K`` must be given.
+    conversion of x_q; x_q may then be None, and ``K`` must be given.  ``prefetch``: an
+    L2 hint, typically the next call's packed weights (a tensor or (tensor, bytes)).
     """
     _cuda(packed, "packed", torch.uint8)
     _cuda(act_scale, "act_scale", torch.float32)
@@ -225,10 +240,11 @@ def bitlinear_forward(x_q, act_scale: torch.Tensor, packed: torch.Tensor,
         need = bitlinear_forward_workspace_bytes(M, N, K)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=packed.device)
+    pf, pf_bytes = _prefetch(prefetch)
     _check("bitlinear_forward", lib().bitlinear_forward(
         _ptr(x_q), _ptr(act_scale), _ptr(x_ops), _ptr(packed), _ptr(w_scale), M, N, K, code, _ptr(y),
         _ptr(acc_debug), _ptr(workspace), 0 if workspace is None else workspace.numel(),
-        int(flags), _stream(stream)))
+        pf, pf_bytes, int(flags), _stream(stream)))
     return y
 
 
@@ -244,10 +260,17 @@ def bitlinear_linear_route(M: int, N: int, K: int) -> int:
     return int(lib().bitlinear_linear_route(M, N, K))
 
 
+def bitlinear_prefill_cluster_size(x_ops, M: int, N: int, K: int) -> int:
+    """CTAs per cluster of the prefill contraction for operands at ``x_ops`` (a tensor or a
+    raw address): 2 only for memory of the current CUDA device; -1 off the prefill route."""
+    addr = x_ops.data_ptr() if isinstance(x_ops, torch.Tensor) else x_ops
+    return int(lib().bitlinear_prefill_cluster_size(ctypes.c_void_p(addr), M, N, K))
+
+
 def bitlinear_linear_forward(x: torch.Tensor, gain, rms_eps: float, packed: torch.Tensor,
                              w_scale: torch.Tensor, out_dtype=torch.bfloat16, y=None, x_q=None,
                              act_scale=None, acc_debug=None, workspace=None, flags: int = 0,
-                             residual: bool = False, stream=None):
+                             residual: bool = False, stream=None, prefetch=None):
     """The BitLinear layer: y [M,N] = dequant(quant(RMSNorm(x)) . W_q^T) from bf16 x [M,K] (CUDA).
 
     ``gain``: RMSNorm weight (bf16 [K]) or None; ``rms_eps < 0`` skips RMSNorm.  ``x_q``
@@ -255,6 +278,8 @@ def bitlinear_linear_forward(x: torch.Tensor, gain, rms_eps: float, packed: torc
     ``residual``: y (bf16) holds the residual on entry and receives y + result.
     One token with K <= 8192 runs as a single kernel; :func:`bitlinear_linear_route`
     tells which kernels a shape takes (the results are the same on every route).
+    ``prefetch``: an L2 hint, typically the next call's packed weights (see
+    :func:`bitlinear_forward`).
     """
     _cuda(x, "x", torch.bfloat16)
     _cuda(packed, "packed", torch.uint8)
@@ -280,7 +305,7 @@ def bitlinear_linear_forward(x: torch.Tensor, gain, rms_eps: float, packed: torc
     _check("bitlinear_linear_forward", lib().bitlinear_linear_forward(
         _ptr(x), _ptr(gain), float(rms_eps), _ptr(packed), _ptr(w_scale), M, N, K, code, _ptr(y),
         _ptr(x_q), _ptr(act_scale), _ptr(acc_debug), _ptr(workspace),
-        0 if workspace is None else workspace.numel(), int(flags), _stream(stream)))
+        0 if workspace is None else workspace.numel(), *_prefetch(prefetch), int(flags), _stream(stream)))
     return y
 
 

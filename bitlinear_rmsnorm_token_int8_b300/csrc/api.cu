@@ -67,6 +67,17 @@ bitlinear_status from_cuda(cudaError_t e) {
   return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
 }
 
+// The caller's L2 prefetch range, its size rounded down to 16 bytes (empty when
+// either is 0 / NULL).
+L2Prefetch prefetch_range(const void* p, size_t bytes) {
+  L2Prefetch pf;
+  if (p && bytes >= 16) {
+    pf.p = static_cast<const uint8_t*>(p);
+    pf.bytes = (uint64_t)(bytes & ~size_t(15));
+  }
+  return pf;
+}
+
 }  // namespace
 
 static std::atomic<uint64_t> g_launches{0};
@@ -106,7 +117,7 @@ const char* bitlinear_status_string(bitlinear_status status) {
   return "unknown status";
 }
 
-int bitlinear_abi_version(void) { return 1; }
+int bitlinear_abi_version(void) { return 2; }
 
 uint64_t bitlinear_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -169,7 +180,8 @@ bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, co
                                    const uint8_t* packed, const float* w_scale, int64_t M,
                                    int64_t N, int64_t K, int out_dtype, void* y,
                                    int32_t* acc_debug, void* workspace, size_t workspace_bytes,
-                                   unsigned flags, void* stream) {
+                                   const void* l2_prefetch, size_t l2_prefetch_bytes, unsigned flags,
+                                   void* stream) {
   if (M < 0 || M > (int64_t(1) << 24) || N < 16 || N % 16 != 0 || N > (int64_t(1) << 24) ||
       K < 128 || K % 128 != 0 || K > 65536)
     return BITLINEAR_ERR_SHAPE;
@@ -180,7 +192,7 @@ bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, co
   if (!act_scale || !packed || !w_scale || !y || (!x_q && !x_ops)) return BITLINEAR_ERR_NULL;
   if ((x_q && !aligned16(x_q)) || (x_ops && !aligned16(x_ops)) || !aligned16(act_scale) ||
       !aligned16(packed) || !aligned16(w_scale) || !aligned16(y) ||
-      (acc_debug && !aligned16(acc_debug)))
+      (acc_debug && !aligned16(acc_debug)) || (l2_prefetch && !aligned16(l2_prefetch)))
     return BITLINEAR_ERR_ALIGN;
   if (!x_ops) {                                   // x_q is converted in the workspace, if needed
     const size_t need = forward_workspace_bytes(M, N, K);
@@ -192,7 +204,7 @@ bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, co
   return from_cuda(launch_forward(x_q, act_scale, static_cast<const uint8_t*>(x_ops), packed,
                                   w_scale, M, N, K, out_dtype, y, acc_debug, workspace,
                                   dev->err_word, (flags & BITLINEAR_FLAG_PDL) != 0,
-                                  static_cast<cudaStream_t>(stream)));
+                                  static_cast<cudaStream_t>(stream), prefetch_range(l2_prefetch, l2_prefetch_bytes)));
 }
 
 namespace {
@@ -216,11 +228,17 @@ int bitlinear_linear_route(int64_t M, int64_t N, int64_t K) {
   return act_ops_prefill(M) ? BITLINEAR_ROUTE_PREFILL : BITLINEAR_ROUTE_DECODE;
 }
 
+int bitlinear_prefill_cluster_size(const void* x_ops, int64_t M, int64_t N, int64_t K) {
+  if (bitlinear_linear_route(M, N, K) != BITLINEAR_ROUTE_PREFILL || !x_ops) return -1;
+  return prefill_cluster(x_ops, N);
+}
+
 bitlinear_status bitlinear_linear_forward(const void* x_bf16, const void* gain_bf16, float rms_eps,
                                           const uint8_t* packed, const float* w_scale, int64_t M,
                                           int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
                                           float* act_scale, int32_t* acc_debug, void* workspace,
-                                          size_t workspace_bytes, unsigned flags, void* stream) {
+                                          size_t workspace_bytes, const void* l2_prefetch,
+                                          size_t l2_prefetch_bytes, unsigned flags, void* stream) {
   if (M < 0 || M > (int64_t(1) << 24) || N < 16 || N % 16 != 0 || N > (int64_t(1) << 24) ||
       K < 128 || K % 128 != 0 || K > 65536)
     return BITLINEAR_ERR_SHAPE;
@@ -231,7 +249,7 @@ bitlinear_status bitlinear_linear_forward(const void* x_bf16, const void* gain_b
   if (!x_bf16 || !packed || !w_scale || !y) return BITLINEAR_ERR_NULL;
   if (!aligned16(x_bf16) || (gain_bf16 && !aligned16(gain_bf16)) || !aligned16(packed) ||
       !aligned16(w_scale) || !aligned16(y) || (x_q && !aligned16(x_q)) || (act_scale && !aligned16(act_scale)) ||
-      (acc_debug && !aligned16(acc_debug)))
+      (acc_debug && !aligned16(acc_debug)) || (l2_prefetch && !aligned16(l2_prefetch)))
     return BITLINEAR_ERR_ALIGN;
   if (!workspace || workspace_bytes < linear_split_bytes(M, K)) return BITLINEAR_ERR_WORKSPACE;
   if (!aligned16(workspace)) return BITLINEAR_ERR_ALIGN;
@@ -241,26 +259,32 @@ bitlinear_status bitlinear_linear_forward(const void* x_bf16, const void* gain_b
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ops = static_cast<uint8_t*>(workspace);
   float* scale = act_scale ? act_scale : reinterpret_cast<float*>(ops + linear_ops_bytes(M, K));
+  const L2Prefetch next = prefetch_range(l2_prefetch, l2_prefetch_bytes);
   if (fused_route(M, N, K))                      // one token: the whole layer in one kernel
     return from_cuda(launch_linear_dp4a(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
                                         rms_eps, packed, w_scale, N, K, out_dtype, y, x_q, act_scale, acc_debug,
-                                        pdl, s));
+                                        pdl, s, next));
+  // Two kernels: the quantization, which starts first, pulls the contraction's
+  // packed weights into L2; the contraction then prefetches the caller's range.
+  L2Prefetch own;
+  own.p = packed;
+  own.bytes = (uint64_t)packed_layout_bytes(N, K);
   if (codes_route(M, N, K)) {
     // a few tokens: the contraction reads the int8 codes (kept in the workspace's
     // operand region unless x_q is given), not the operand form
     int8_t* codes = x_q ? x_q : reinterpret_cast<int8_t*>(ops);
     cudaError_t e = launch_quant_act(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
-                                     rms_eps, M, K, codes, scale, nullptr, pdl, s);
+                                     rms_eps, M, K, codes, scale, nullptr, pdl, s, own);
     if (e != cudaSuccess) return from_cuda(e);
     return from_cuda(launch_forward(codes, scale, nullptr, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
-                                    nullptr, dev->err_word, true, s));
+                                    nullptr, dev->err_word, true, s, next));
   }
   cudaError_t e = launch_quant_act(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
-                                   rms_eps, M, K, x_q, scale, ops, pdl, s);
+                                   rms_eps, M, K, x_q, scale, ops, pdl, s, act_ops_prefill(M) ? L2Prefetch{} : own);
   if (e != cudaSuccess) return from_cuda(e);
   // the contraction follows a kernel of this library: overlapping with it is safe
   return from_cuda(launch_forward(nullptr, scale, ops, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
-                                  nullptr, dev->err_word, true, s));
+                                  nullptr, dev->err_word, true, s, next));
 }
 
 bitlinear_status bitlinear_get_device_error(void* stream) {

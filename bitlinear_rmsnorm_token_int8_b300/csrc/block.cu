@@ -88,43 +88,57 @@ extern "C" bitlinear_status bitlinear_block_forward(const bitlinear_layer* layer
   bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
   cudaError_t e = cudaSuccess;
   // per projection: int8 codes in the operand region for the CUDA-core contraction
-  // (one or two tokens), or the tensor-core operand form
+  // (one or two tokens), or the tensor-core operand form.  Every contraction pulls
+  // the packed weights of the projection after it into L2 while it runs, so the
+  // weight stream continues across the launches; the first quantization pulls in
+  // the first projection's.
   int8_t* const codes_buf = reinterpret_cast<int8_t*>(w.ops);
-  auto quant = [&](const uint16_t* in, int64_t ld, const float* glu, const void* gain, int64_t N, int64_t K) {
+  auto quant = [&](const uint16_t* in, int64_t ld, const float* glu, const void* gain, int64_t N, int64_t K,
+                   L2Prefetch pf) {
     const bool codes = codes_route(M, N, K);
     if (e == cudaSuccess)
       e = launch_quant_act_ex(in, ld, glu, static_cast<const uint16_t*>(gain), rms_eps, M, K,
-                              codes ? codes_buf : nullptr, w.scale, codes ? nullptr : w.ops, pdl, s);
+                              codes ? codes_buf : nullptr, w.scale, codes ? nullptr : w.ops, pdl, s, pf);
     pdl = true;                         // everything after the first kernel is ours
   };
-  auto forward = [&](const uint8_t* packed, const float* wscale, int64_t N, int64_t K, int out_dtype, void* y) {
+  auto forward = [&](const uint8_t* packed, const float* wscale, int64_t N, int64_t K, int out_dtype, void* y,
+                     L2Prefetch next) {
     const bool codes = codes_route(M, N, K);
     if (e == cudaSuccess)
       e = launch_forward(codes ? codes_buf : nullptr, w.scale, codes ? nullptr : w.ops, packed, wscale, M, N, K,
-                         out_dtype, y, nullptr, nullptr, err, true, s);
+                         out_dtype, y, nullptr, nullptr, err, true, s, next);
+  };
+  auto weights = [](const uint8_t* packed, int64_t N, int64_t K) {
+    L2Prefetch pf;
+    pf.p = packed;
+    pf.bytes = (uint64_t)packed_layout_bytes(N, K);
+    return pf;
   };
   // one projection on bf16 rows `in` (pitch ld): for one token one kernel (RMSNorm,
   // quantization and contraction together), else quantization, then the contraction
   auto layer = [&](const uint16_t* in, int64_t ld, const void* gain, const uint8_t* packed, const float* wscale,
-                   int64_t N, int64_t K, int out_dtype, void* y) {
+                   int64_t N, int64_t K, int out_dtype, void* y, L2Prefetch own, L2Prefetch next) {
     if (fused_route(M, N, K)) {
       if (e == cudaSuccess)
         e = launch_linear_dp4a(in, static_cast<const uint16_t*>(gain), rms_eps, packed, wscale, N, K, out_dtype, y,
-                               nullptr, nullptr, nullptr, pdl, s);
+                               nullptr, nullptr, nullptr, pdl, s, next);
       pdl = true;
       return;
     }
-    quant(in, ld, nullptr, gain, N, K);
-    forward(packed, wscale, N, K, out_dtype, y);
+    quant(in, ld, nullptr, gain, N, K, own);
+    forward(packed, wscale, N, K, out_dtype, y, next);
   };
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const bitlinear_layer& L = layers[l];
-    layer(x, H, L.gain_qkv, L.qkv, L.qkv_scale, NQKV, H, BITLINEAR_OUT_BF16, w.qkv);
+    const L2Prefetch w_o = weights(L.o, H, H), w_gu = weights(L.gate_up, 2 * F, H), w_down = weights(L.down, H, F);
+    const L2Prefetch w_next = l + 1 < n_layers ? weights(layers[l + 1].qkv, NQKV, H) : L2Prefetch{};
+    layer(x, H, L.gain_qkv, L.qkv, L.qkv_scale, NQKV, H, BITLINEAR_OUT_BF16, w.qkv,
+          l == 0 ? weights(L.qkv, NQKV, H) : L2Prefetch{}, w_o);
     // the query slice stands in for attention
-    layer(w.qkv, NQKV, L.gain_o, L.o, L.o_scale, H, H, BITLINEAR_OUT_BF16_ADD, x_bf16);
-    layer(x, H, L.gain_gate_up, L.gate_up, L.gate_up_scale, 2 * F, H, BITLINEAR_OUT_F32, w.gu);
-    quant(nullptr, F, w.gu, L.gain_down, H, F);                   // h = bf16(relu(gate)^2 * up)
-    forward(L.down, L.down_scale, H, F, BITLINEAR_OUT_BF16_ADD, x_bf16);
+    layer(w.qkv, NQKV, L.gain_o, L.o, L.o_scale, H, H, BITLINEAR_OUT_BF16_ADD, x_bf16, L2Prefetch{}, w_gu);
+    layer(x, H, L.gain_gate_up, L.gate_up, L.gate_up_scale, 2 * F, H, BITLINEAR_OUT_F32, w.gu, L2Prefetch{}, w_down);
+    quant(nullptr, F, w.gu, L.gain_down, H, F, L2Prefetch{});     // h = bf16(relu(gate)^2 * up)
+    forward(L.down, L.down_scale, H, F, BITLINEAR_OUT_BF16_ADD, x_bf16, w_next);
   }
   return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
 }

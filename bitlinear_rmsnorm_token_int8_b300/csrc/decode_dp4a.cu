@@ -47,6 +47,8 @@ struct DecodeDp4aParams {
   const float* w_scale;
   void* y;
   int32_t* acc_debug;
+  const uint8_t* pf;         // L2 prefetch of the caller (or null)
+  uint64_t pf_bytes;
   int M, N, K, nseg, Np, out_dtype;
 };
 
@@ -106,6 +108,7 @@ __global__ void __launch_bounds__(kDThreads) decode_dp4a_kernel(const DecodeDp4a
   }
   const bool nv = row < p.N;
   const float wsn = nv ? __ldg(p.w_scale + row) : 0.0f;
+  if (threadIdx.x < 32) l2_prefetch_share(p.pf, p.pf_bytes, threadIdx.x, 32);
   pdl_launch_dependents();
   pdl_wait();                                // x_q, act_scale and y follow the stream order
 
@@ -211,6 +214,8 @@ struct LinearDp4aParams {
   int8_t* x_q;               // [K] out, or null
   float* act_scale;          // [1] out, or null
   int32_t* acc_debug;
+  const uint8_t* pf;         // L2 prefetch of the caller (or null)
+  uint64_t pf_bytes;
   int N, K, nseg, Np, out_dtype;
 };
 
@@ -250,6 +255,7 @@ __global__ void __launch_bounds__(512) linear_dp4a_kernel(const LinearDp4aParams
     gv[hv] = (p.gain && tid < U && v < V) ? __ldg(p.gain + v) : kOnes;
   }
   if (tid < U && (tid & 3) == 0) prefetch_l2(p.x + 2 * tid);
+  if (tid < 32) l2_prefetch_share(p.pf, p.pf_bytes, tid, 32);
   pdl_launch_dependents();
   pdl_wait();                                // x and y follow the stream order
 
@@ -282,9 +288,8 @@ __global__ void __launch_bounds__(512) linear_dp4a_kernel(const LinearDp4aParams
     }
   }
   block_stats(amax, hi, lo, tid, T >> 5, s_max, s_ss, &s_m, &s_sum);
-  const float m = fmaxf(s_m, 1e-8f);
-  const float sq = __fdiv_rn(127.0f, m);
-  const float sigma = act_sigma(m, s_sum, p.K, p.rms_eps);
+  const RowQuant rq = row_quant(s_m, s_sum, p.K, p.rms_eps);
+  const float sigma = rq.sigma;
 
   // codes of this unit (zero past K), staged permuted for the dot products
   if (tid < p.nseg * 32) {
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(512) linear_dp4a_kernel(const LinearDp4aParams
       unpack8(gv[hv], gf);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int q = quant_code(__fmul_rn(xf[j], gf[j]), sq, m);
+        const int q = row_code(__fmul_rn(xf[j], gf[j]), rq);
         w[2 * hv + (j >> 2)] |= (uint32_t)(q & 0xff) << (8 * (j & 3));
       }
     }
@@ -381,7 +386,8 @@ bool fused_route(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rms_eps, const uint8_t* packed,
                                const float* w_scale, int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
-                               float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream) {
+                               float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream,
+                               L2Prefetch pf) {
   if (!fused_route(1, N, K)) return cudaErrorInvalidValue;
   LinearDp4aParams p = {};
   p.x = reinterpret_cast<const uint4*>(x);
@@ -393,6 +399,8 @@ cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rm
   p.x_q = x_q;
   p.act_scale = act_scale;
   p.acc_debug = acc_debug;
+  p.pf = pf.p;
+  p.pf_bytes = pf.bytes;
   p.N = (int)N;
   p.K = (int)K;
   p.nseg = (int)(act_ops_kpad(K) / 512);
@@ -413,7 +421,7 @@ cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rm
 
 cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
                                const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
-                               void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream) {
+                               void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream, L2Prefetch pf) {
   if (!codes_route(M, N, K)) return cudaErrorInvalidValue;
   const size_t smem = decode_dp4a_smem(M, K);
   DecodeDp4aParams p = {};
@@ -423,6 +431,8 @@ cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const 
   p.w_scale = w_scale;
   p.y = y;
   p.acc_debug = acc_debug;
+  p.pf = pf.p;
+  p.pf_bytes = pf.bytes;
   p.M = (int)M;
   p.N = (int)N;
   p.K = (int)K;

@@ -81,6 +81,8 @@ struct DecodeTcParams {
   void* y;
   int32_t* acc_debug;
   int* dev_err;
+  const uint8_t* pf;         // L2 prefetch of the caller (or null)
+  uint64_t pf_bytes;
   int M, N, out_dtype;
   int nseg, ntiles16;
   int S, G, NS, stage_bytes;
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
         const int slot = st % p.NS, round = st / p.NS;
         if (round >= 1) {
           if (!waited) {
+            l2_prefetch_share(p.pf, p.pf_bytes, 0, 1);   // after this CTA's first weight copies
             pdl_wait();
             waited = true;
             for (int d = st - deferred; d < st; ++d) issue_x(d);
@@ -215,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
         else ++deferred;
       }
       if (!waited) {
+        l2_prefetch_share(p.pf, p.pf_bytes, 0, 1);
         pdl_wait();
         for (int d = st - deferred; d < st; ++d) issue_x(d);
       }
@@ -479,7 +483,7 @@ cudaError_t launch_act_ops_from_codes(const int8_t* x_q, int64_t M, int64_t K, u
 cudaError_t launch_decode_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
                              const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
                              void* y, int32_t* acc_debug, int* dev_err, bool pdl,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, L2Prefetch pf) {
   const DecodePlan pl = decode_plan(M, N, K, num_sms());
   if (!decode_plan_ok(pl)) return cudaErrorInvalidValue;
   DecodeTcParams p = {};
@@ -490,6 +494,8 @@ cudaError_t launch_decode_tc(const uint8_t* x_ops, const float* act_scale, const
   p.y = y;
   p.acc_debug = acc_debug;
   p.dev_err = dev_err;
+  p.pf = pf.p;
+  p.pf_bytes = pf.bytes;
   p.M = (int)M;
   p.N = (int)N;
   p.out_dtype = out_dtype;

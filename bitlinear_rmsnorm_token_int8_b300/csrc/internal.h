@@ -31,6 +31,15 @@ inline int64_t packed_nseg(int64_t K) { return (K + kSegK - 1) / kSegK; }
 inline int64_t packed_rows(int64_t N) { return (N + 15) / 16 * 16; }
 inline int64_t packed_layout_bytes(int64_t N, int64_t K) { return packed_rows(N) * packed_nseg(K) * 128; }
 
+// A device range that a call's kernels ask the copy engine to pull into L2 while
+// they run (typically the packed weights of the call that follows on the stream).
+// It is only a cache hint: nothing reads it into registers or shared memory, and
+// L2 is the point of coherence, so it can never make a kernel see stale data.
+struct L2Prefetch {
+  const uint8_t* p = nullptr;
+  uint64_t bytes = 0;
+};
+
 // ---- pack_weights --------------------------------------------------------
 // Workspace layout (bytes): [0, 2048) 256 uint64 exponent bins of sum|W|,
 // [2048, 2056) gamma and d = fl32(gamma + eps) as two floats.
@@ -45,13 +54,13 @@ cudaError_t launch_pack_weights(const float* W, int64_t N, int64_t K, float eps,
 // x_ops: optional tensor-core operand planes of the codes (act_ops.cuh), or nullptr.
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,
                              int64_t K, int8_t* x_q, float* act_scale, uint8_t* x_ops, bool pdl,
-                             cudaStream_t stream);
+                             cudaStream_t stream, L2Prefetch pf = {});
 
 // Same with a row pitch `ld` (elements, a multiple of 8) or, if `glu` is set, the
 // ReLU^2-gated rows of fp32 [gate | up] (x unused).  x_q may be null.
 cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu, const uint16_t* gain,
                                 float rms_eps, int64_t M, int64_t K, int8_t* x_q, float* act_scale,
-                                uint8_t* x_ops, bool pdl, cudaStream_t stream);
+                                uint8_t* x_ops, bool pdl, cudaStream_t stream, L2Prefetch pf = {});
 
 // ---- activation operands ---------------------------------------------------
 size_t act_ops_bytes(int64_t M, int64_t K);
@@ -65,7 +74,7 @@ size_t forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint8_t* x_ops,
                            const uint8_t* packed, const float* w_scale, int64_t M, int64_t N,
                            int64_t K, int out_dtype, void* y, int32_t* acc_debug, void* workspace,
-                           int* dev_err, bool pdl, cudaStream_t stream);
+                           int* dev_err, bool pdl, cudaStream_t stream, L2Prefetch pf = {});
 
 // Decode contraction (M <= kDecodeMaxM) on tcgen05: launch plan and launcher.
 struct DecodePlan {
@@ -84,7 +93,7 @@ bool decode_plan_ok(const DecodePlan& pl);
 cudaError_t launch_decode_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
                              const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
                              void* y, int32_t* acc_debug, int* dev_err, bool pdl,
-                             cudaStream_t stream);
+                             cudaStream_t stream, L2Prefetch pf = {});
 
 // Decode contraction for one or two tokens on the CUDA cores (int8 dot products),
 // reading the int8 codes x_q; shared memory per CTA from decode_dp4a_smem.
@@ -95,21 +104,26 @@ size_t decode_dp4a_smem(int64_t M, int64_t K);
 bool codes_route(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
                                const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
-                               void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream);
+                               void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream,
+                               L2Prefetch pf = {});
 
 // The whole layer (RMSNorm + quantization + contraction) for one token in one kernel,
 // when K <= 8192 and the codes route applies; x_q and act_scale outputs optional.
 bool fused_route(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rms_eps, const uint8_t* packed,
                                const float* w_scale, int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
-                               float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream);
+                               float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream,
+                               L2Prefetch pf = {});
 
 int num_sms();
 
 // ---- tensor maps and the prefill contraction ---------------------------------
 
-// Tokens per tile of the prefill contraction (256, or 128 when that fills more SMs).
-int prefill_tile_tokens(int64_t M, int64_t N, int sms);
+// CTAs per cluster of the prefill contraction for operands at x_ops (2 only when
+// x_ops is memory of the current device and N spans two weight blocks), and tokens
+// per tile (256, or 128 when that fills more SMs) for that cluster size.
+int prefill_cluster(const void* x_ops, int64_t N);
+int prefill_tile_tokens(int64_t M, int64_t N, int CL, int sms);
 
 cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, const uint8_t* packed,
                               const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,

@@ -417,13 +417,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 
 }  // namespace
 
+// True when p points into device memory of the calling thread's current device.
+// Anything else (host memory, managed memory, a peer GPU's memory reached through
+// unified addressing, or a pointer the runtime does not know) is not.
+bool local_device_memory(const void* p) {
+  int dev = -1;
+  cudaPointerAttributes a = {};
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+// CTAs per cluster of the prefill contraction: 2 (the activation blocks multicast
+// to both CTAs of a cluster; measured: 2 beats 1 and 4) when there are at least two
+// weight blocks and the operands lie in the current device's own memory, so that a
+// multicast copy only ever reads this GPU's memory; 1 otherwise.
+int prefill_cluster(const void* x_ops, int64_t N) {
+  const int64_t nwb = (N + kTileW - 1) / kTileW;
+  return nwb >= 2 && local_device_memory(x_ops) ? 2 : 1;
+}
+
 // Tokens per tile: 128 when that takes less time in tile-rounds of the persistent
 // grid, a 128-token tile costing 0.74 of a 256-token one (measured on B300 over
 // 2B and 8B shapes at 256-2048 tokens: half the MMAs and operand bytes, but the
 // same weight decode and a fixed cost per tile).
-int prefill_tile_tokens(int64_t M, int64_t N, int sms) {
+int prefill_tile_tokens(int64_t M, int64_t N, int CL, int sms) {
   const int64_t nwb = (N + kTileW - 1) / kTileW;
-  const int64_t CL = nwb >= 2 ? 2 : 1;
   const int64_t ncl = sms / CL > 0 ? sms / CL : 1;
   const int64_t g = (nwb + CL - 1) / CL;
   const int64_t r256 = (g * ((M + 255) / 256) + ncl - 1) / ncl;
@@ -437,9 +458,9 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
                               cudaStream_t stream) {
   const int64_t Kp = act_ops_kpad(K);
   const int64_t nwb = (N + kTileW - 1) / kTileW;
-  const int CL = nwb >= 2 ? 2 : 1;             // measured: 2 beats 1 and 4
+  const int CL = prefill_cluster(x_ops, N);
   const int sms = num_sms();
-  const int TT = prefill_tile_tokens(M, N, sms);
+  const int TT = prefill_tile_tokens(M, N, CL, sms);
   PrefillParams p = {};
   p.packed = packed;
   p.x_ops = x_ops;

@@ -89,7 +89,8 @@ typedef enum bitlinear_status {
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bitlinear_status_string(bitlinear_status status);
 
-/* ABI version, currently 1. */
+/* ABI version, currently 2 (2 added the l2_prefetch arguments of bitlinear_forward
+ * and bitlinear_linear_forward). */
 int bitlinear_abi_version(void);
 
 /* Number of kernels this library has enqueued in this process so far (all devices,
@@ -100,7 +101,9 @@ uint64_t bitlinear_kernel_launches(void);
 /* 1. weights                                                                */
 /* ------------------------------------------------------------------------ */
 
-/* Bytes of the packed ternary matrix: N * K / 4. */
+/* Bytes of the packed ternary matrix in the tile-major layout below: Np * Kp / 4,
+ * with Np = N rounded up to a multiple of 16 and Kp = K rounded up to a multiple
+ * of 512 (the padding holds zero codes); 0 for shapes bitlinear_pack_weights rejects. */
 size_t bitlinear_packed_bytes(int64_t N, int64_t K);
 
 /* Bytes of scratch that bitlinear_pack_weights needs (independent of N and K). */
@@ -190,8 +193,11 @@ size_t bitlinear_act_ops_bytes(int64_t M, int64_t K);
  *
  * Because r > 0 is one number per row, x_q equals the codes of x*g computed
  * exactly: the kernel decides every code from exact binary32 products, so x_q is
- * bit-exact whatever the summation order of mean(x^2).  A row whose max|x*g| is
- * below 1e-8 uses 1e-8 as its max (all-zero rows give zero codes).
+ * bit-exact whatever the summation order of mean(x^2).  As activation_quant
+ * clamps its scale, a row whose max|n_k| (formed as fl32(max|x*g| * r), r =
+ * fl32(1 / fl32(sqrt(fl32(fl32(mean x^2) + rms_eps))))) is below 1e-8 uses 1e-8 as
+ * its max: its codes are rint(fl32(fl32(x g r) * fl32(127 / 1e-8))) and act_scale
+ * = 1e-8 / 127 (all-zero rows give zero codes).
  *
  * x_bf16   [M,K] bf16 tokens.  Must be finite, with |x| <= 2^60 and |x*g| <= 2^100
  *          (beyond that the fp32 squares or products may overflow).
@@ -243,17 +249,30 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * workspace >= bitlinear_forward_workspace_bytes(M,N,K) bytes of device scratch
  *           when x_ops is NULL (may be NULL when that is 0, or with x_ops).
  *           Contents on entry do not matter.
+ * l2_prefetch, l2_prefetch_bytes  a range of device memory of the current
+ *           device (16-byte aligned; the size is rounded down to 16 bytes), or
+ *           NULL / 0: typically the packed weights of the call that follows on
+ *           the stream.  The decode kernels (M <= 32) ask the copy engine to
+ *           pull it into L2 while they run, so that a chain of decode calls
+ *           keeps HBM streaming weights across its launches; the prefill
+ *           contraction ignores it.  It is a cache hint only: the range is not
+ *           read otherwise, results do not depend on it, and it may be written
+ *           by other work at any time.
  * flags     0 or BITLINEAR_FLAG_PDL.
  *
- * Exactness: the kernels contract on the tensor cores with e4m3 operands; each
- * code enters as two exact e4m3 values (see bitlinear_act_ops_bytes) and every
- * fp32 accumulator stays an integer below 2^24 in magnitude (at most 128 K <= 2^23),
- * so acc is the exact integer sum.
+ * Exactness: every route forms acc as the exact integer sum.  With x_q given and
+ * M <= BITLINEAR_CODES_MAX_M (see there for the exact shape rule) a CUDA-core
+ * kernel contracts the int8 codes with int32 dot products (|acc| <= 127 K < 2^31).
+ * Otherwise the tensor cores contract e4m3 operands: each code enters as two
+ * exact e4m3 values (see bitlinear_act_ops_bytes) and every fp32 accumulator
+ * stays an integer below 2^24 in magnitude (at most 128 K <= 2^23).  Both give
+ * the same acc and y bit for bit.
  */
 bitlinear_status bitlinear_forward(const int8_t *x_q, const float *act_scale, const void *x_ops,
                                    const uint8_t *packed, const float *w_scale,
                                    int64_t M, int64_t N, int64_t K, int out_dtype, void *y,
                                    int32_t *acc_debug, void *workspace, size_t workspace_bytes,
+                                   const void *l2_prefetch, size_t l2_prefetch_bytes,
                                    unsigned flags, void *stream);
 
 /* Bytes of scratch that bitlinear_linear_forward needs: the operand form of the
@@ -279,6 +298,20 @@ size_t bitlinear_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int bitlinear_linear_route(int64_t M, int64_t N, int64_t K);
 
 /*
+ * CTAs per thread-block cluster that the prefill contraction (the
+ * BITLINEAR_ROUTE_PREFILL kernel of bitlinear_forward and
+ * bitlinear_linear_forward) uses for operands at x_ops: 2 when x_ops is device
+ * memory of the calling thread's current device and N spans at least two
+ * 128-row weight blocks, 1 otherwise.  With 2, one copy of each activation block
+ * from x_ops is multicast to both CTAs of the cluster; the check keeps such
+ * copies to this GPU's own memory (host, managed or peer memory is never their
+ * source).  -1 when the shape does not take the prefill route or x_ops is NULL.
+ * The result depends only on the arguments and the current device; nothing is
+ * enqueued.
+ */
+int bitlinear_prefill_cluster_size(const void *x_ops, int64_t M, int64_t N, int64_t K);
+
+/*
  * The whole BitLinear layer in one call ([P4-code] BitLinear.forward: RMSNorm,
  * activation_quant, the ternary product and the rescale; [P1-impl]
  * bitlinear_forward(x, W_packed, s)).  For one token with K <= 8192 a single
@@ -295,6 +328,10 @@ int bitlinear_linear_route(int64_t M, int64_t N, int64_t K);
  * workspace >= bitlinear_linear_workspace_bytes(M,N,K) bytes of device scratch
  *           (required on every route; the one-kernel route leaves it untouched).
  *           Contents on entry do not matter.
+ * l2_prefetch, l2_prefetch_bytes  as bitlinear_forward (the next call's weights,
+ *           or NULL / 0).  On the two-kernel routes of decode sizes the
+ *           quantization kernel, which starts first, also pulls this call's own
+ *           packed weights into L2.
  * flags     0 or BITLINEAR_FLAG_PDL (the first launch may overlap the work
  *           already on the stream).
  */
@@ -302,7 +339,8 @@ bitlinear_status bitlinear_linear_forward(const void *x_bf16, const void *gain_b
                                           const uint8_t *packed, const float *w_scale, int64_t M,
                                           int64_t N, int64_t K, int out_dtype, void *y, int8_t *x_q,
                                           float *act_scale, int32_t *acc_debug, void *workspace,
-                                          size_t workspace_bytes, unsigned flags, void *stream);
+                                          size_t workspace_bytes, const void *l2_prefetch,
+                                          size_t l2_prefetch_bytes, unsigned flags, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* 4. the linear stack of a BitNet b1.58 transformer                         */

@@ -76,10 +76,22 @@ def test_linear_route(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.bitlinear_abi_version() == 1
+    assert L.bitlinear_abi_version() == 2
     for s in range(11):
         assert L.bitlinear_status_string(s)
     assert L.bitlinear_status_string(99) == b"unknown status"
+
+
+def test_prefill_cluster_size_needs_local_device_memory(L):
+    # the cluster-of-2 prefill kernel multicasts activation blocks; it is chosen only for
+    # operands in the current device's own memory, never for a host address
+    host = np.zeros(1 << 16, dtype=np.uint8)
+    addr = host.ctypes.data
+    assert L.bitlinear_prefill_cluster_size(addr, 2048, 14336, 4096) == 1
+    assert L.bitlinear_prefill_cluster_size(addr, 2048, 128, 4096) == 1
+    assert L.bitlinear_prefill_cluster_size(addr, 8, 14336, 4096) == -1      # decode route
+    assert L.bitlinear_prefill_cluster_size(None, 2048, 14336, 4096) == -1
+    assert L.bitlinear_prefill_cluster_size(addr, 2048, 100, 4096) == -1     # rejected shape
 
 
 def test_sizes(L):
@@ -98,8 +110,8 @@ def test_sizes(L):
 
 
 def _fwd(L, x=FAKE, s=FAKE, ops=None, p=FAKE, w=FAKE, M=4, N=512, K=256, dt=0, y=FAKE, acc=None,
-         ws=FAKE, wsb=1 << 30, flags=0):
-    return L.bitlinear_forward(x, s, ops, p, w, M, N, K, dt, y, acc, ws, wsb, flags, None)
+         ws=FAKE, wsb=1 << 30, flags=0, pf=None, pfb=0):
+    return L.bitlinear_forward(x, s, ops, p, w, M, N, K, dt, y, acc, ws, wsb, pf, pfb, flags, None)
 
 
 def test_forward_argument_errors(L):
@@ -120,12 +132,14 @@ def test_forward_argument_errors(L):
     assert _fwd(L, dt=7) == ERR_DTYPE
     assert _fwd(L, x=FAKE + 4) == ERR_ALIGN
     assert _fwd(L, acc=FAKE + 8) == ERR_ALIGN
+    assert _fwd(L, pf=FAKE + 8, pfb=4096) == ERR_ALIGN      # the L2 prefetch range must be 16-byte aligned
     # valid arguments: only now is the device consulted (none here, or not sm_103)
     import torch
     if not torch.cuda.is_available():
         assert _fwd(L) == ERR_DEVICE
         assert _fwd(L, x=None, ops=FAKE, ws=None, flags=1) == ERR_DEVICE   # x_ops alone suffices
         assert _fwd(L, M=2, ws=None) == ERR_DEVICE            # one or two tokens: x_q alone suffices
+        assert _fwd(L, pf=FAKE, pfb=100) == ERR_DEVICE        # any size: rounded down to 16 bytes
 
 
 def test_quant_act_argument_errors(L):
@@ -147,8 +161,9 @@ def test_quant_act_argument_errors(L):
 
 def test_linear_forward_argument_errors(L):
     def lf(x=FAKE, g=None, p=FAKE, w=FAKE, M=4, N=512, K=256, dt=1, y=FAKE, xq=None, sc=None, acc=None,
-           ws=None, wsb=0, flags=0):
-        return L.bitlinear_linear_forward(x, g, 1e-5, p, w, M, N, K, dt, y, xq, sc, acc, ws, wsb, flags, None)
+           ws=None, wsb=0, flags=0, pf=None, pfb=0):
+        return L.bitlinear_linear_forward(x, g, 1e-5, p, w, M, N, K, dt, y, xq, sc, acc, ws, wsb, pf, pfb, flags,
+                                          None)
     assert lf(x=None) == ERR_NULL
     assert lf(p=None) == ERR_NULL
     assert lf(M=0, x=None, p=None, w=None, y=None) == OK
@@ -159,6 +174,7 @@ def test_linear_forward_argument_errors(L):
     assert lf(flags=8) == ERR_FLAGS
     assert lf(g=FAKE + 2) == ERR_ALIGN
     assert lf(xq=FAKE + 8) == ERR_ALIGN
+    assert lf(pf=FAKE + 4, pfb=64) == ERR_ALIGN
     # quantization into the workspace (operand form + scales), then the contraction
     assert L.bitlinear_linear_workspace_bytes(1, 2560, 2560) >= L.bitlinear_act_ops_bytes(1, 2560) + 4
     need = L.bitlinear_linear_workspace_bytes(64, 512, 256)

@@ -163,3 +163,47 @@ def test_linear_one_token_fused(K, N, gain, rms):
     torch.cuda.synchronize()
     assert torch.equal(r["xq"], xq2) and torch.equal(r["sc"], sc2)
     assert torch.equal(r["acc"], acc2) and torch.equal(r["y"], y2)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 2560, 2560),      # the one-kernel layer
+    (1, 4096, 14336),     # quantization + the int8-code kernel
+    (2, 3840, 2560),      # two tokens on the int8-code kernel
+    (8, 3840, 2560),      # quantization + tcgen05 decode
+    (16, 1040, 4096),
+    (64, 512, 1536),      # prefill (takes no prefetch)
+])
+def test_l2_prefetch_hint_changes_nothing(M, N, K):
+    # the l2_prefetch range (here the packed weights of a second matrix, as in a chain of
+    # calls) is a cache hint: codes, accumulators and outputs are bit-identical with it
+    x = synth.activations(M, K, seed=M + N).cuda()
+    g = synth.rms_gains(K, seed=K).cuda()
+    packed, w_scale, _ = bl.bitlinear_pack_weights(synth.latent_weights(N, K, seed=N).cuda())
+    nxt, _, _ = bl.bitlinear_pack_weights(synth.latent_weights(2 * N, K, seed=N + 1).cuda())
+    outs = []
+    for pf in (None, nxt, (nxt, 1000)):
+        acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        y = bl.bitlinear_linear_forward(x, g, RMS_EPS, packed, w_scale, out_dtype=torch.float32, acc_debug=acc,
+                                        flags=bl.FLAG_PDL, prefetch=pf)
+        xq, sc = bl.bitlinear_quant_act(x, g, RMS_EPS)
+        acc2 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        y2 = bl.bitlinear_forward(xq, sc, packed, w_scale, out_dtype=torch.float32, acc_debug=acc2, prefetch=pf)
+        torch.cuda.synchronize()
+        outs.append((y.cpu(), acc.cpu(), y2.cpu(), acc2.cpu()))
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert torch.equal(a, b)
+    assert torch.equal(outs[0][1], outs[0][3])
+
+
+def test_prefill_cluster_size_by_memory_kind():
+    # clusters of two (one multicast copy of each activation block for both CTAs) only
+    # for operands in this device's own memory
+    d = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    assert bl.bitlinear_prefill_cluster_size(d, 2048, 14336, 4096) == 2
+    assert bl.bitlinear_prefill_cluster_size(d, 2048, 128, 4096) == 1      # one weight block
+    assert bl.bitlinear_prefill_cluster_size(d, 16, 14336, 4096) == -1     # decode route
+    pinned = torch.empty(1 << 20, dtype=torch.uint8, pin_memory=True)
+    assert bl.bitlinear_prefill_cluster_size(pinned, 2048, 14336, 4096) == 1
+    pageable = torch.empty(1 << 20, dtype=torch.uint8)
+    assert bl.bitlinear_prefill_cluster_size(pageable, 2048, 14336, 4096) == 1
