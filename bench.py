@@ -285,10 +285,12 @@ def traffic_record(workload, kernel_srcs):
 
 def kernel_sources():
     csrc = os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc")
-    return [os.path.join(csrc, f) for f in ("decode_dp4a.cu", "quant_math.cuh", "decode_tc.cu", "device_util.cuh")]
+    return [os.path.join(csrc, f) for f in ("decode_cc.cu", "quant_math.cuh", "decode_tc.cu", "device_util.cuh")]
 
 
 def timed_replays(torch, graph, stream, steps):
+    """ms per replay of `graph`, by CUDA events on `stream` (the caller makes it current)."""
+    assert torch.cuda.current_stream() == stream
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(steps):
@@ -447,22 +449,23 @@ def measure_decode(bl, synth, torch, dev, workload, layers, steps, warmup, e2e=T
     hbm, _, peak_src = measured_peaks()
     per_shape, launch_ms, launch_bytes = [], [], []
     for M, p, g in shape_graphs:
-        per_launch = timed_replays(torch, g, stream, steps) / layers
+        with torch.cuda.stream(stream):                  # replay on the stream the events record on
+            per_launch = timed_replays(torch, g, stream, steps) / layers
         alg = alg_bytes(M, p)
         gbs = alg / (per_launch * 1e-3) / 1e9
         per_shape.append({"tokens": M, "projection": p.name, "K": p.K, "N": p.N,
-                          "kernel": {bl.ROUTE_FUSED: "linear_dp4a_kernel", bl.ROUTE_CODES: "decode_dp4a_kernel"}.get(
-                              route(M, p), "decode_tc_kernel"),
+                          "kernel": {bl.ROUTE_FUSED: "CUDA-core layer kernel (linear_dp4a / decode_cc)",
+                                     bl.ROUTE_CODES: "CUDA-core codes kernel (decode_dp4a / decode_cc)"}.get(
+                                         route(M, p), "decode_tc_kernel"),
                           "launch_us": per_launch * 1e3, "alg_bytes": alg, "alg_gbs": gbs, "frac": gbs / hbm})
         launch_ms.extend([per_launch] * layers)
         launch_bytes.extend([alg] * layers)
     achieved = sum(launch_bytes) / (sum(launch_ms) * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic_record(workload, kernel_sources()), "peak_source": peak_src,
-                "kernel": "the decode contraction + dequant of each projection (per_shape[].kernel): at M = 1 "
-                          "linear_dp4a_kernel (the whole layer: RMSNorm, quantization, int8-code contraction) "
-                          "for K <= 8192 and decode_dp4a_kernel on the int8 codes above, at M = 4 and 16 "
-                          "decode_tc_kernel (tcgen05)",
+                "kernel": "the decode contraction + dequant of each projection (per_shape[].kernel): for one "
+                          "or two tokens decode_cc_kernel (CUDA cores; for K <= 8192 the whole layer: RMSNorm, "
+                          "quantization, int8-code contraction), for more decode_tc_kernel (tcgen05)",
                 "timing": "CUDA events around K replays of a graph of the layers' launches per (M, projection)",
                 "alg_bytes_per_launch": sum(launch_bytes) / len(launch_bytes),
                 "avg_launch_us": sum(launch_ms) / len(launch_ms) * 1e3,

@@ -38,7 +38,7 @@ OUT_BF16 = 1
 OUT_BF16_ADD = 2
 FLAG_PDL = 1
 # BITLINEAR_CODES_MAX_M: bitlinear_forward given x_q contracts on the int8 codes (x_ops
-# unused, no workspace) for one token, and for two with K <= 4096 and N K <= 2^26
+# unused, no workspace) for one token, and for two whose staged codes fit in shared memory
 CODES_MAX_M = 2
 STATUS = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_DTYPE", 5: "ERR_DEVICE",
           6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_WORKSPACE", 9: "ERR_NONFINITE", 10: "ERR_FLAGS"}

@@ -174,7 +174,7 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return forward_workspace_bytes(M, N, K);
 }
 
-static_assert(kDp4aMaxM == BITLINEAR_CODES_MAX_M, "the header's CODES_MAX_M is the codes kernel's limit");
+static_assert(kCodesMaxM == BITLINEAR_CODES_MAX_M, "the header's CODES_MAX_M is the codes kernel's limit");
 
 bitlinear_status bitlinear_forward(const int8_t* x_q, const float* act_scale, const void* x_ops,
                                    const uint8_t* packed, const float* w_scale, int64_t M,
@@ -261,26 +261,22 @@ bitlinear_status bitlinear_linear_forward(const void* x_bf16, const void* gain_b
   float* scale = act_scale ? act_scale : reinterpret_cast<float*>(ops + linear_ops_bytes(M, K));
   const L2Prefetch next = prefetch_range(l2_prefetch, l2_prefetch_bytes);
   if (fused_route(M, N, K))                      // one token: the whole layer in one kernel
-    return from_cuda(launch_linear_dp4a(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
-                                        rms_eps, packed, w_scale, N, K, out_dtype, y, x_q, act_scale, acc_debug,
-                                        pdl, s, next));
-  // Two kernels: the quantization, which starts first, pulls the contraction's
-  // packed weights into L2; the contraction then prefetches the caller's range.
-  L2Prefetch own;
-  own.p = packed;
-  own.bytes = (uint64_t)packed_layout_bytes(N, K);
+    return from_cuda(launch_layer_cc(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
+                                     rms_eps, packed, w_scale, M, N, K, out_dtype, y, x_q, act_scale, acc_debug,
+                                     pdl, s, next));
+  // Two kernels: quantization, then the contraction, which prefetches the caller's range.
   if (codes_route(M, N, K)) {
     // a few tokens: the contraction reads the int8 codes (kept in the workspace's
     // operand region unless x_q is given), not the operand form
     int8_t* codes = x_q ? x_q : reinterpret_cast<int8_t*>(ops);
     cudaError_t e = launch_quant_act(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
-                                     rms_eps, M, K, codes, scale, nullptr, pdl, s, own);
+                                     rms_eps, M, K, codes, scale, nullptr, pdl, s);
     if (e != cudaSuccess) return from_cuda(e);
     return from_cuda(launch_forward(codes, scale, nullptr, packed, w_scale, M, N, K, out_dtype, y, acc_debug,
                                     nullptr, dev->err_word, true, s, next));
   }
   cudaError_t e = launch_quant_act(static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gain_bf16),
-                                   rms_eps, M, K, x_q, scale, ops, pdl, s, act_ops_prefill(M) ? L2Prefetch{} : own);
+                                   rms_eps, M, K, x_q, scale, ops, pdl, s);
   if (e != cudaSuccess) return from_cuda(e);
   // the contraction follows a kernel of this library: overlapping with it is safe
   return from_cuda(launch_forward(nullptr, scale, ops, packed, w_scale, M, N, K, out_dtype, y, acc_debug,

@@ -120,8 +120,8 @@ extern "C" bitlinear_status bitlinear_block_forward(const bitlinear_layer* layer
                    int64_t N, int64_t K, int out_dtype, void* y, L2Prefetch own, L2Prefetch next) {
     if (fused_route(M, N, K)) {
       if (e == cudaSuccess)
-        e = launch_linear_dp4a(in, static_cast<const uint16_t*>(gain), rms_eps, packed, wscale, N, K, out_dtype, y,
-                               nullptr, nullptr, nullptr, pdl, s, next);
+        e = launch_layer_cc(in, static_cast<const uint16_t*>(gain), rms_eps, packed, wscale, M, N, K, out_dtype, y,
+                            nullptr, nullptr, nullptr, pdl, s, next);
       pdl = true;
       return;
     }

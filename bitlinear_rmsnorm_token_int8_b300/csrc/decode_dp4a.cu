@@ -357,19 +357,8 @@ cudaError_t launch_fused_ks(const LinearDp4aParams& p, int T, bool pdl, cudaStre
                        : launch_fused_cfg<KS, 8>(p, T, pdl, stream);
 }
 
-}  // namespace
-
 size_t decode_dp4a_smem(int64_t M, int64_t K) {
   return (size_t)((M <= 1 ? 1 : 2) * (act_ops_kpad(K) / 512) * kSegPitch);
-}
-
-// Measured on B300 against the tensor-core kernel (PDL-chained launches of the 2B and
-// 8B projections): this kernel is faster for every shape at one token; at two, for
-// K <= 4096 up to 16 MiB of packed weights (2B projections 13-36 % faster, the 8B
-// gate+up of 56 MiB 6 % slower); slower from three tokens on.
-bool codes_route(int64_t M, int64_t N, int64_t K) {
-  return (M == 1 || (M == 2 && K <= 4096 && N * K <= (int64_t(1) << 26))) &&
-         decode_dp4a_smem(M, K) <= 227 * 1024;
 }
 
 // Lanes per (row, chunk): the fewest that leave a lane at most five segments (more
@@ -380,15 +369,25 @@ int dp4a_split(int nseg) {
   return ks;
 }
 
-bool fused_route(int64_t M, int64_t N, int64_t K) {
-  return M == 1 && K <= kFusedMaxSeg * 512 && codes_route(M, N, K);
+}  // namespace
+
+// Shapes this file's kernels take: the codes kernel one token (any K) or two with
+// K <= 4096 and N K <= 2^26, within its shared memory; the layer kernel one token
+// with K <= 8192.
+bool dp4a_codes_ok(int64_t M, int64_t N, int64_t K) {
+  return (M == 1 || (M == 2 && K <= 4096 && N * K <= (int64_t(1) << 26))) &&
+         decode_dp4a_smem(M, K) <= 227 * 1024;
+}
+
+bool dp4a_layer_ok(int64_t M, int64_t N, int64_t K) {
+  return M == 1 && K <= kFusedMaxSeg * 512 && dp4a_codes_ok(M, N, K);
 }
 
 cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rms_eps, const uint8_t* packed,
                                const float* w_scale, int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
                                float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream,
                                L2Prefetch pf) {
-  if (!fused_route(1, N, K)) return cudaErrorInvalidValue;
+  if (!dp4a_layer_ok(1, N, K)) return cudaErrorInvalidValue;
   LinearDp4aParams p = {};
   p.x = reinterpret_cast<const uint4*>(x);
   p.gain = reinterpret_cast<const uint4*>(gain);
@@ -422,7 +421,7 @@ cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rm
 cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
                                const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
                                void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream, L2Prefetch pf) {
-  if (!codes_route(M, N, K)) return cudaErrorInvalidValue;
+  if (!dp4a_codes_ok(M, N, K)) return cudaErrorInvalidValue;
   const size_t smem = decode_dp4a_smem(M, K);
   DecodeDp4aParams p = {};
   p.packed = packed;

@@ -19,7 +19,7 @@ cudaError_t launch_forward(const int8_t* x_q, const float* act_scale, const uint
   // a few tokens with their int8 codes at hand: the CUDA-core kernel, which needs no
   // operand form
   if (x_q && codes_route(M, N, K))
-    return launch_decode_dp4a(x_q, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug, pdl, stream, pf);
+    return launch_codes_cc(x_q, act_scale, packed, w_scale, M, N, K, out_dtype, y, acc_debug, pdl, stream, pf);
   if (!x_ops) {
     uint8_t* ops = static_cast<uint8_t*>(workspace);
     cudaError_t e = launch_act_ops_from_codes(x_q, M, K, ops, pdl, stream);

@@ -95,25 +95,40 @@ cudaError_t launch_decode_tc(const uint8_t* x_ops, const float* act_scale, const
                              void* y, int32_t* acc_debug, int* dev_err, bool pdl,
                              cudaStream_t stream, L2Prefetch pf = {});
 
-// Decode contraction for one or two tokens on the CUDA cores (int8 dot products),
-// reading the int8 codes x_q; shared memory per CTA from decode_dp4a_smem.
-constexpr int64_t kDp4aMaxM = 2;
-size_t decode_dp4a_smem(int64_t M, int64_t K);
-// True when bitlinear_forward with x_q takes that kernel: M == 1, or M == 2 with
-// K <= 4096 and N K <= 2^26, and the tokens' staged codes fit in shared memory.
+// Decode contraction for one or two tokens on the CUDA cores (int8 dot products,
+// one persistent CTA per SM), reading the int8 codes x_q; shared memory per CTA
+// from decode_cc_smem (0: the shape does not fit).
+constexpr int64_t kCodesMaxM = 2;
+size_t decode_cc_smem(int64_t M, int64_t K);
+// True when bitlinear_forward with x_q takes that kernel: 1 <= M <= kCodesMaxM and
+// the tokens' staged codes and the weight ring fit in shared memory.
 bool codes_route(int64_t M, int64_t N, int64_t K);
-cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
-                               const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
-                               void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream,
-                               L2Prefetch pf = {});
+cudaError_t launch_codes_cc(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
+                            const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
+                            void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream,
+                            L2Prefetch pf = {});
 
 // The whole layer (RMSNorm + quantization + contraction) for one token in one kernel,
 // when K <= 8192 and the codes route applies; x_q and act_scale outputs optional.
 bool fused_route(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_layer_cc(const uint16_t* x, const uint16_t* gain, float rms_eps, const uint8_t* packed,
+                            const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype, void* y,
+                            int8_t* x_q, float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream,
+                            L2Prefetch pf = {});
+
+// The CUDA-core kernels of many small CTAs (decode_dp4a.cu), which launch_codes_cc
+// and launch_layer_cc take for matrices below kCcMinBytes of packed weights: there
+// they finish sooner in a chain of dependent launches than the persistent kernel.
+constexpr int64_t kCcMinBytes = int64_t(12) << 20;
+bool dp4a_codes_ok(int64_t M, int64_t N, int64_t K);
+bool dp4a_layer_ok(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_decode_dp4a(const int8_t* x_q, const float* act_scale, const uint8_t* packed,
+                               const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype,
+                               void* y, int32_t* acc_debug, bool pdl, cudaStream_t stream, L2Prefetch pf);
 cudaError_t launch_linear_dp4a(const uint16_t* x, const uint16_t* gain, float rms_eps, const uint8_t* packed,
                                const float* w_scale, int64_t N, int64_t K, int out_dtype, void* y, int8_t* x_q,
                                float* act_scale, int32_t* acc_debug, bool pdl, cudaStream_t stream,
-                               L2Prefetch pf = {});
+                               L2Prefetch pf);
 
 int num_sms();
 

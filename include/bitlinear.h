@@ -75,14 +75,13 @@ typedef enum bitlinear_status {
 #define BITLINEAR_FLAG_PDL 1u
 
 /*
- * Largest token count for which bitlinear_forward, given x_q, can contract on
- * the int8 codes directly (a CUDA-core kernel with int8 dot products; x_ops is
- * then not read and no workspace is needed): it does so for one token (any K)
- * and for two tokens with K <= 4096 and N K <= 2^26 (at most 16 MiB of packed
- * weights), the shapes where it was measured faster than the tensor-core
- * kernel; bitlinear_forward_workspace_bytes returns 0 exactly then.  Otherwise,
- * or with x_ops alone, the tensor-core kernels run on the operand form.
- * Results are identical.
+ * Largest token count for which bitlinear_forward, given x_q, contracts on the
+ * int8 codes directly (a persistent CUDA-core kernel with int8 dot products;
+ * x_ops is then not read and no workspace is needed).  It does so for M = 1
+ * (every K) and M = 2 (K <= 37376), where the tokens' staged codes fit in
+ * shared memory; bitlinear_forward_workspace_bytes returns 0 exactly then.
+ * Otherwise, or with x_ops alone, the tensor-core kernels run on the operand
+ * form.  Results are identical.
  */
 #define BITLINEAR_CODES_MAX_M 2
 
@@ -284,10 +283,11 @@ size_t bitlinear_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   BITLINEAR_ROUTE_FUSED    one kernel: RMSNorm, quantization and the int8-code
  *                            contraction together (one token, K <= 8192);
  *   BITLINEAR_ROUTE_CODES    quantization to int8 codes, then the CUDA-core
- *                            contraction on them (two tokens with small K, or one
- *                            token with K > 8192);
+ *                            contraction on them (one token with K > 8192, or
+ *                            two tokens);
  *   BITLINEAR_ROUTE_DECODE   quantization to the operand form, then the tcgen05
- *                            decode contraction (up to 32 tokens);
+ *                            decode contraction (3 to 32 tokens, or two where
+ *                            their codes do not fit the CUDA-core kernel);
  *   BITLINEAR_ROUTE_PREFILL  quantization to the operand form, then the tcgen05
  *                            prefill contraction (more tokens).
  * -1 for shapes the call rejects. */
@@ -329,9 +329,7 @@ int bitlinear_prefill_cluster_size(const void *x_ops, int64_t M, int64_t N, int6
  *           (required on every route; the one-kernel route leaves it untouched).
  *           Contents on entry do not matter.
  * l2_prefetch, l2_prefetch_bytes  as bitlinear_forward (the next call's weights,
- *           or NULL / 0).  On the two-kernel routes of decode sizes the
- *           quantization kernel, which starts first, also pulls this call's own
- *           packed weights into L2.
+ *           or NULL / 0); the contraction kernel issues it.
  * flags     0 or BITLINEAR_FLAG_PDL (the first launch may overlap the work
  *           already on the stream).
  */

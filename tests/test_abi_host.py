@@ -53,8 +53,9 @@ def test_codes_route_needs_no_workspace(L):
     # bitlinear_forward given x_q: no scratch where the int8-code kernel takes it
     ws = L.bitlinear_forward_workspace_bytes
     assert ws(1, 2560, 2560) == 0 and ws(1, 4096, 65536) == 0 and ws(2, 3840, 2560) == 0
-    assert ws(2, 28672, 4096) == L.bitlinear_act_ops_bytes(2, 4096)     # 56 MiB of weights: tcgen05
-    assert ws(3, 2560, 2560) == L.bitlinear_act_ops_bytes(3, 2560)
+    assert ws(2, 28672, 4096) == 0 and ws(2, 4096, 37376) == 0
+    assert ws(2, 4096, 65536) == L.bitlinear_act_ops_bytes(2, 65536)   # two tokens' codes do not fit
+    assert ws(3, 2560, 2560) == L.bitlinear_act_ops_bytes(3, 2560)     # three tokens: tcgen05
     assert ws(64, 2560, 2560) == L.bitlinear_act_ops_bytes(64, 2560)
 
 
@@ -62,11 +63,13 @@ def test_linear_route(L):
     route = L.bitlinear_linear_route
     assert route(1, 2560, 2560) == bl.ROUTE_FUSED            # one token, K <= 8192: one kernel
     assert route(1, 4096, 8192) == bl.ROUTE_FUSED
-    assert route(1, 4096, 14336) == bl.ROUTE_CODES           # one token, longer K: quant + codes kernel
-    assert route(2, 3840, 2560) == bl.ROUTE_CODES
-    assert route(2, 28672, 4096) == bl.ROUTE_DECODE          # two tokens, 56 MiB of weights: tcgen05
-    assert route(2, 2560, 6912) == bl.ROUTE_DECODE           # two tokens, K > 4096
+    assert route(1, 4096, 14336) == bl.ROUTE_CODES           # longer K: quant + codes kernel
+    assert route(2, 3840, 2560) == bl.ROUTE_CODES            # two tokens: quant + codes kernel
+    assert route(2, 28672, 4096) == bl.ROUTE_CODES
+    assert route(2, 4096, 14336) == bl.ROUTE_CODES
+    assert route(2, 4096, 65536) == bl.ROUTE_DECODE          # two tokens' codes do not fit: tcgen05
     assert route(3, 2560, 2560) == bl.ROUTE_DECODE
+    assert route(4, 28672, 4096) == bl.ROUTE_DECODE
     assert route(32, 2560, 2560) == bl.ROUTE_DECODE
     assert route(33, 2560, 2560) == bl.ROUTE_PREFILL
     assert route(0, 2560, 2560) == -1 and route(1, 24, 2560) == -1 and route(1, 2560, 100) == -1

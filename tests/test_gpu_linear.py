@@ -148,17 +148,19 @@ def test_linear_residual_and_pdl_chain(M):
     assert np.all(np.abs(got - (r0f + o_y2)) <= 2.0 ** -7 * scale + 1e-30)
 
 
-@pytest.mark.parametrize("K,N,gain,rms", [(128, 144, True, True), (1152, 272, False, True), (2560, 3840, True, True),
-                                          (6912, 2560, True, False), (8192, 400, True, True)])
-def test_linear_one_token_fused(K, N, gain, rms):
-    # one token, K <= 8192: RMSNorm, quantization and the contraction in one kernel.  Its
-    # codes, scale, accumulators and outputs equal the oracle's and, bit for bit, those of
-    # the two-kernel path (quantization, then the contraction on the int8 codes)
-    assert bl.bitlinear_linear_route(1, N, K) == bl.ROUTE_FUSED
+@pytest.mark.parametrize("M,K,N,gain,rms", [
+    (1, 128, 144, True, True), (1, 1152, 272, False, True), (1, 2560, 3840, True, True),
+    (1, 6912, 2560, True, False), (1, 8192, 400, True, True), (1, 4096, 28672, True, True),
+    (1, 2560, 13824, False, True)])
+def test_linear_one_token_fused(M, K, N, gain, rms):
+    # one token, K <= 8192: RMSNorm, quantization and the contraction in one kernel.
+    # Its codes, scales, accumulators and outputs equal the oracle's and, bit for bit, those
+    # of the two-kernel path (quantization, then the contraction on the int8 codes)
+    assert bl.bitlinear_linear_route(M, N, K) == bl.ROUTE_FUSED
     eps = RMS_EPS if rms else -1.0
-    r = run_linear(1, N, K, torch.float32, seed=K + N, gain=gain, rms_eps=eps, flags=bl.FLAG_PDL)
+    r = run_linear(M, N, K, torch.float32, seed=K + N + M, gain=gain, rms_eps=eps, flags=bl.FLAG_PDL)
     xq2, sc2 = bl.bitlinear_quant_act(r["x"].cuda(), None if r["g"] is None else r["g"].cuda(), eps)
-    acc2 = torch.empty((1, N), dtype=torch.int32, device="cuda")
+    acc2 = torch.empty((M, N), dtype=torch.int32, device="cuda")
     y2 = bl.bitlinear_forward(xq2, sc2, r["packed"], r["w_scale"], out_dtype=torch.float32, acc_debug=acc2)
     torch.cuda.synchronize()
     assert torch.equal(r["xq"], xq2) and torch.equal(r["sc"], sc2)

@@ -292,7 +292,7 @@ def test_forward_matches_oracle(M, N, K, dt):
 
 
 @pytest.mark.parametrize("M,K", [(1, 128), (1, 640), (2, 640), (1, 4096), (2, 4096), (1, 6912), (1, 14336),
-                                 (1, 65536)])
+                                 (1, 65536), (2, 14336), (2, 37376)])
 def test_codes_route_equals_operand_route(M, K):
     # one or two tokens given x_q run on the int8-code (CUDA-core) kernel; given only the
     # operand form, on the tensor cores: same accumulators and outputs, both equal to the
@@ -310,6 +310,30 @@ def test_codes_route_equals_operand_route(M, K):
         y2 = bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=dt, acc_debug=acc2, x_ops=ops, K=K)
         torch.cuda.synchronize()
         assert torch.equal(acc1, acc2) and torch.equal(y1, y2)
+    o_xq, _ = oracle.act_quant(synth.bf16_bits(x), None, RMS_EPS)
+    _, _, o_wq = oracle.pack_weights(W.numpy())
+    assert (xq.cpu().numpy() == o_xq).all()
+    assert (acc1.cpu().numpy() == oracle.ternary_matmul(o_xq, o_wq)).all()
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 14336, 4096), (2, 4096, 28672), (2, 14336, 4096), (1, 65536, 2048),
+                                   (2, 37376, 1408)])
+def test_codes_route_large_matrices(M, K, N):
+    # from 12 MiB of packed weights the int8-code route runs the persistent CUDA-core
+    # kernel (one CTA per SM, weights streamed through shared memory): same accumulators
+    # and outputs as the tensor cores on the operand form, and as the oracle
+    x = synth.activations(M, K, seed=7 * M + K)
+    W = synth.latent_weights(N, K, seed=N + K)
+    packed, w_scale, gamma = bl.bitlinear_pack_weights(W.cuda())
+    assert bl.bitlinear_packed_bytes(N, K) >= 12 << 20
+    xq, sc, ops = bl.bitlinear_quant_act(x.cuda(), None, RMS_EPS, x_ops=True)
+    assert bl.bitlinear_forward_workspace_bytes(M, N, K) == 0
+    acc1 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    acc2 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y1 = bl.bitlinear_forward(xq, sc, packed, w_scale, out_dtype=torch.float32, acc_debug=acc1, flags=bl.FLAG_PDL)
+    y2 = bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=torch.float32, acc_debug=acc2, x_ops=ops, K=K)
+    torch.cuda.synchronize()
+    assert torch.equal(acc1, acc2) and torch.equal(y1, y2)
     o_xq, _ = oracle.act_quant(synth.bf16_bits(x), None, RMS_EPS)
     _, _, o_wq = oracle.pack_weights(W.numpy())
     assert (xq.cpu().numpy() == o_xq).all()
