@@ -22,6 +22,10 @@ and the composition of the steps.  Each function names the passage it follows:
 * [P5-block] "BitNet 1-bit LLM Inference Framework", section "A Full BitNet
             Transformer Block" (q/k/v/o and gate/up/down projections, residual
             adds around the attention and the FFN).
+* [P5-aq]   same page, BitLinear.activation_quantize (per-tensor scale, Q_b = 128).
+* [P2-wr]   "BitNet-2B-4T: Inside the 2B-Parameter, 4T-Token 1-Bit LLM", section
+            "Weight Representation: Ternary + Scale, Not Pure Binary"
+            (per-output-channel scaling W_bit x s, s in R^d).
 
 Parity pins: every function here is pinned by ``tests/test_oracle.py`` (hand-worked
 values in ``tests/golden/worked_examples.json``, including the bf16 rounding of
@@ -84,6 +88,8 @@ def _load():
         lib.oracle_ternary_matmul_at.restype = None
         lib.oracle_dequant.argtypes = [P, P, P, I64, I64, P]
         lib.oracle_dequant.restype = None
+        lib.oracle_act_quant_per_tensor.argtypes = [P, I64, I64, P, P]
+        lib.oracle_act_quant_per_tensor.restype = None
         _lib = lib
     return _lib
 
@@ -187,6 +193,20 @@ def unpack_codes(packed: np.ndarray, K: int, strict: bool = True) -> np.ndarray:
     return q
 
 
+def pack_weights_per_channel(w: np.ndarray, eps: np.float32 = EPS_W):
+    """[P2-wr] per-output-channel scale s in R^N: the absmean of [P4-eq] item 1 taken
+    over each output row, gamma_n = (1/K) sum_k |W_nk| (the exact mean rounded once to
+    binary32), and W_q[n] = Clip(Round(W[n] / (gamma_n + eps)), -1, 1).  READING: the
+    page gives the per-channel form but not how s is obtained; the row absmean is the
+    plainest reading that keeps the page's ternarization.  The page stores s in FP16;
+    here it stays binary32 like the per-tensor gamma.
+    Returns (packed [N, K/4], gammas float32 [N], w_q int8 [N, K])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    gammas = np.array([absmean_gamma(row) for row in w], dtype=np.float32)
+    q = np.stack([ternarize(row, g, eps) for row, g in zip(w, gammas)]) if len(w) else np.zeros(w.shape, np.int8)
+    return pack_codes(q), gammas, q
+
+
 def pack_weights(w: np.ndarray, eps: np.float32 = EPS_W):
     """absmean gamma, ternary codes and packed bytes of one latent matrix W [N,K] fp32."""
     gamma = absmean_gamma(w)
@@ -217,6 +237,20 @@ def act_quant(x_bits: np.ndarray, gain_bits: np.ndarray | None, rms_eps: float):
     sigma = np.empty(M, dtype=np.float64)
     lib.oracle_act_quant(_ptr(x_bits), _ptr(gain_bits) if gain_bits is not None else None,
                          float(rms_eps), M, K, _ptr(xq), _ptr(sigma))
+    return xq, sigma
+
+
+def act_quant_per_tensor(x_bits: np.ndarray):
+    """[P5-aq] per-tensor absmax quantization with Q_b = 128 (no RMSNorm).
+
+    x_bits: [M,K] uint16 bf16 patterns.  Returns (x_q int8 [M,K] in [-128, 127],
+    sigma float64 [M], every entry max|x| / 128)."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    xq = np.empty((M, K), dtype=np.int8)
+    sigma = np.empty(M, dtype=np.float64)
+    lib.oracle_act_quant_per_tensor(_ptr(x_bits), M, K, _ptr(xq), _ptr(sigma))
     return xq, sigma
 
 

@@ -306,3 +306,39 @@ void oracle_dequant(const int32_t *acc, const double *sigma, const double *w_sca
         for (n = 0; n < N; ++n)
             y[t * N + n] = (double)acc[t * N + n] * sigma[t] * w_scale[n];
 }
+
+/* ------------------------------------------------------------------------- */
+/* per-tensor activation quantization with Q_b = 128                         */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * [P5-aq] "BitNet 1-bit LLM Inference Framework", BitLinear.activation_quantize
+ * (the variant of that page): one scale for the whole tensor,
+ *   gamma = max_{t,k} |x|,   x_q = Round(Clip(x * Q_b / (gamma + 1e-8), -Q_b, Q_b - 1))
+ * with Q_b = 2^(8-1) = 128; the clip comes before the rounding, as in the page's
+ * code, so codes lie in [-128, 127]; Round is nearest, ties to even.  No
+ * RMSNorm.  The page's tensors are binary32, so the quotient is formed in
+ * binary32: x * 128 is exact, gamma + 1e-8 is one binary32 rounding and the
+ * division one more; that rounded quotient decides the code.  The dequant
+ * factor of every token is sigma = gamma / 128 (the page multiplies the
+ * integer product by w_scale * gamma / 2^7).
+ */
+void oracle_act_quant_per_tensor(const uint16_t *x, int64_t M, int64_t K, int8_t *xq, double *sigma)
+{
+    int64_t i, n = M * K;
+    double g = 0.0;
+    float d;
+    for (i = 0; i < n; ++i) {
+        double a = fabs(bf16_to_double(x[i]));
+        if (a > g) g = a;
+    }
+    d = (float)g + 1e-8f;
+    for (i = 0; i < n; ++i) {
+        float xs = (float)bf16_to_double(x[i]) * 128.0f;
+        float t = xs / d;
+        if (t < -128.0f) t = -128.0f;
+        if (t > 127.0f) t = 127.0f;
+        xq[i] = (int8_t)rintf(t);
+    }
+    for (i = 0; i < M; ++i) sigma[i] = g / 128.0;
+}

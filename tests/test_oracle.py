@@ -473,3 +473,87 @@ def test_block_layer_matches_dense_fp64_recomputation():
     x2 = oracle.bf16_bits_to_f64(xb).astype(np.float32)
     expect = oracle.f32_to_bf16_bits(x2 + lin(h, layer["gain_down"], layer["down"], layer["down_scale"]))
     assert (oracle.block_layer(x, layer, 1e-5) == expect).all()
+
+
+# ---------------------------------------------------------------------------
+# scale-granularity variants: per-output-channel weight scale, per-tensor Q_b = 128
+# ---------------------------------------------------------------------------
+
+def test_pack_per_channel_worked_example():
+    ex = GOLDEN["weights_per_channel_2x4"]
+    W = np.array(ex["W"], dtype=np.float32)
+    packed, gammas, wq = oracle.pack_weights_per_channel(W, np.float32(ex["eps"]))
+    assert gammas.tolist() == ex["gamma"]
+    assert wq.tolist() == ex["w_q"]
+    assert packed.tolist() == ex["packed"]
+    # the per-tensor packing of the same matrix zeroes the small row
+    _, g, q = oracle.pack_weights(W, np.float32(ex["eps"]))
+    assert float(g) == ex["per_tensor_gamma"] and q.tolist() == ex["per_tensor_w_q"]
+
+
+def test_pack_per_channel_rows_are_one_row_matrices():
+    # each row's scale and codes are those of that row packed alone (a 1 x K matrix),
+    # whose per-tensor absmean is pinned above
+    rng = np.random.default_rng(21)
+    W = (rng.standard_normal((9, 40)) * np.exp2(rng.integers(-6, 4, (9, 1)))).astype(np.float32)
+    _, gammas, wq = oracle.pack_weights_per_channel(W)
+    for n in range(9):
+        _, g, q = oracle.pack_weights(W[n:n + 1])
+        assert gammas[n] == g and (wq[n] == q[0]).all()
+
+
+def test_pack_per_channel_equals_per_tensor_for_rows_of_equal_magnitudes():
+    # rows that are sign flips and permutations of one row share its mean |W|: one scale
+    rng = np.random.default_rng(22)
+    base = (rng.standard_normal(64) * 0.02).astype(np.float32)
+    W = np.stack([rng.permutation(base) * rng.choice([-1.0, 1.0], 64).astype(np.float32) for _ in range(6)])
+    _, gammas, wq = oracle.pack_weights_per_channel(W)
+    _, g, q = oracle.pack_weights(W)
+    assert (gammas == g).all() and (wq == q).all()
+
+
+def test_pack_per_channel_row_scaling_by_powers_of_two():
+    # with eps = 0, scaling row n by 2^j scales its gamma by 2^j exactly and keeps its codes
+    rng = np.random.default_rng(23)
+    W = (rng.standard_normal((5, 96)) * 0.02).astype(np.float32)
+    s = np.exp2(np.array([-3, 0, 2, 5, -1], dtype=np.float32))[:, None]
+    _, g1, q1 = oracle.pack_weights_per_channel(W, np.float32(0.0))
+    _, g2, q2 = oracle.pack_weights_per_channel((W * s).astype(np.float32), np.float32(0.0))
+    assert (g2 == g1 * s[:, 0]).all() and (q1 == q2).all()
+
+
+@pytest.mark.parametrize("key", ["act_per_tensor_q128", "act_per_tensor_tiny"])
+def test_act_quant_per_tensor_worked_examples(key):
+    ex = GOLDEN[key]
+    xb = bf16(ex["x"])
+    assert (bf16_bits_to_f64(xb) == np.array(ex["x"])).all()
+    xq, sigma = oracle.act_quant_per_tensor(xb)
+    assert xq.tolist() == ex["x_q"]
+    want = ex["sigma"] if "sigma" in ex else 2.0 ** ex["sigma_log2"]
+    assert (sigma == want).all()
+
+
+def test_act_quant_per_tensor_dyadic_bruteforce():
+    # with max|x| = 2^j (j >= -2: 1e-8 is below half an ulp of 2^j) the 1e-8 vanishes in
+    # binary32 and x 128 / 2^j is exact: the codes are Round(Clip(x 128 / 2^j, -128, 127))
+    # in exact rationals
+    rng = np.random.default_rng(24)
+    for trial in range(40):
+        M, K = int(rng.integers(1, 5)), int(rng.integers(1, 48))
+        j = int(rng.integers(-2, 8))
+        x = (rng.uniform(-1, 1, (M, K)) * 2.0**j).astype(np.float32)
+        x.flat[int(rng.integers(0, M * K))] = (2.0**j) * (1 if trial % 2 else -1)
+        xb = f32_to_bf16_bits(x)
+        xv = bf16_bits_to_f64(xb)
+        xq, sigma = oracle.act_quant_per_tensor(xb)
+        g = Fraction(2) ** j
+        for t in range(M):
+            for k in range(K):
+                v = Fraction(float(xv[t, k])) * 128 / g
+                v = min(max(v, Fraction(-128)), Fraction(127))
+                assert xq[t, k] == round(v)
+        assert (sigma == float(g) / 128).all()
+    # one scale for the whole tensor: a row's codes depend on the other rows
+    x = np.array([[1.0, 0.5], [4.0, -0.25]], dtype=np.float32)
+    xq, _ = oracle.act_quant_per_tensor(f32_to_bf16_bits(x))
+    assert xq[0].tolist() == [32, 16]
