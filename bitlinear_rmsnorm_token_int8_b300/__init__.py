@@ -31,6 +31,8 @@ __all__ = [
     "bitlinear_block_forward", "bitlinear_block_workspace_bytes", "pack_stacked", "LAYER_FIELDS",
     "bitlinear_linear_forward", "bitlinear_linear_workspace_bytes", "CODES_MAX_M", "bitlinear_linear_route",
     "ROUTE_FUSED", "ROUTE_CODES", "ROUTE_DECODE", "ROUTE_PREFILL", "bitlinear_prefill_cluster_size",
+    "bitlinear_pack_weights_per_channel", "bitlinear_quant_act_per_tensor",
+    "bitlinear_quant_act_per_tensor_workspace_bytes",
 ]
 
 OUT_F32 = 0
@@ -80,6 +82,12 @@ def lib() -> ctypes.CDLL:
         L.bitlinear_act_ops_bytes.restype = SZ
         L.bitlinear_quant_act.argtypes = [P, P, F, I64, I64, P, P, P, U, P]
         L.bitlinear_quant_act.restype = I
+        L.bitlinear_pack_weights_per_channel.argtypes = [P, I64, I64, F, P, P, P]
+        L.bitlinear_pack_weights_per_channel.restype = I
+        L.bitlinear_quant_act_per_tensor_workspace_bytes.argtypes = [I64]
+        L.bitlinear_quant_act_per_tensor_workspace_bytes.restype = SZ
+        L.bitlinear_quant_act_per_tensor.argtypes = [P, I64, I64, P, P, P, P, SZ, U, P]
+        L.bitlinear_quant_act_per_tensor.restype = I
         L.bitlinear_forward_workspace_bytes.argtypes = [I64, I64, I64]
         L.bitlinear_forward_workspace_bytes.restype = SZ
         L.bitlinear_forward.argtypes = [P, P, P, P, P, I64, I64, I64, I, P, P, P, SZ, P, SZ, U, P]
@@ -180,6 +188,47 @@ def bitlinear_pack_weights(W: torch.Tensor, eps: float = 1e-5, packed=None, w_sc
         _ptr(W), N, K, float(eps), _ptr(packed), _ptr(w_scale), _ptr(gamma), _ptr(workspace),
         workspace.numel(), _stream(stream)))
     return packed, w_scale, gamma
+
+
+def bitlinear_pack_weights_per_channel(W: torch.Tensor, eps: float = 1e-5, packed=None, w_scale=None,
+                                       stream=None):
+    """Ternarize + pack W [N,K] fp32 (CUDA) with one absmean per output row.
+    Returns (packed, w_scale) with w_scale[n] = gamma_n."""
+    _cuda(W, "W", torch.float32)
+    N, K = W.shape
+    if packed is None:
+        packed = torch.empty(max(bitlinear_packed_bytes(N, K), 16), dtype=torch.uint8, device=W.device)
+    if w_scale is None:
+        w_scale = torch.empty(N, dtype=torch.float32, device=W.device)
+    _check("bitlinear_pack_weights_per_channel", lib().bitlinear_pack_weights_per_channel(
+        _ptr(W), N, K, float(eps), _ptr(packed), _ptr(w_scale), _stream(stream)))
+    return packed, w_scale
+
+
+def bitlinear_quant_act_per_tensor_workspace_bytes(M: int) -> int:
+    return int(lib().bitlinear_quant_act_per_tensor_workspace_bytes(M))
+
+
+def bitlinear_quant_act_per_tensor(x: torch.Tensor, x_q=None, act_scale=None, x_ops=None, workspace=None,
+                                   flags: int = 0, stream=None):
+    """Per-tensor absmax quantization with Q_b = 128 of x [M,K] bf16 (CUDA), no RMSNorm.
+    ``x_ops`` as in :func:`bitlinear_quant_act`.  Returns (x_q, act_scale[, x_ops])."""
+    _cuda(x, "x", torch.bfloat16)
+    M, K = x.shape
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if act_scale is None:
+        act_scale = torch.empty(max(M, 1) + 3, dtype=torch.float32, device=x.device)[:M]
+    want_ops = x_ops is not None
+    if x_ops is True:
+        x_ops = torch.empty(max(bitlinear_act_ops_bytes(M, K), 16), dtype=torch.uint8, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(bitlinear_quant_act_per_tensor_workspace_bytes(M), 256), dtype=torch.uint8,
+                                device=x.device)
+    _check("bitlinear_quant_act_per_tensor", lib().bitlinear_quant_act_per_tensor(
+        _ptr(x), M, K, _ptr(x_q), _ptr(act_scale), _ptr(x_ops) if want_ops else None, _ptr(workspace),
+        workspace.numel(), int(flags), _stream(stream)))
+    return (x_q, act_scale, x_ops) if want_ops else (x_q, act_scale)
 
 
 def bitlinear_quant_act(x: torch.Tensor, gain=None, rms_eps: float = 1e-5, x_q=None,

@@ -169,6 +169,44 @@ bitlinear_status bitlinear_quant_act(const void* x_bf16, const void* gain_bf16, 
                                     static_cast<cudaStream_t>(stream)));
 }
 
+bitlinear_status bitlinear_pack_weights_per_channel(const float* W, int64_t N, int64_t K, float eps,
+                                                    uint8_t* packed, float* w_scale, void* stream) {
+  if (!W || !packed || !w_scale) return BITLINEAR_ERR_NULL;
+  if (N < 1 || K < 4 || K % 4 != 0 || N * K >= (int64_t(1) << 32) || !(eps >= 0.0f))
+    return BITLINEAR_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(packed) || !aligned16(w_scale)) return BITLINEAR_ERR_ALIGN;
+  const DeviceState* dev = current_device();
+  if (!dev) return BITLINEAR_ERR_DEVICE;
+  return from_cuda(launch_pack_weights_per_channel(W, N, K, eps, packed, w_scale, dev->err_word,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+size_t bitlinear_quant_act_per_tensor_workspace_bytes(int64_t M) {
+  if (M < 0) return 0;
+  return (size_t)((4 * M + 255) / 256 * 256);
+}
+
+bitlinear_status bitlinear_quant_act_per_tensor(const void* x_bf16, int64_t M, int64_t K, int8_t* x_q,
+                                                float* act_scale, void* x_ops, void* workspace,
+                                                size_t workspace_bytes, unsigned flags, void* stream) {
+  if (M < 0 || M > (int64_t(1) << 31) - 1 || K < 8 || K > 65536 || K % 8 != 0)
+    return BITLINEAR_ERR_SHAPE;
+  if (flags & ~kKnownFlags) return BITLINEAR_ERR_FLAGS;
+  if (M == 0) return BITLINEAR_OK;
+  if (!x_bf16 || !x_q || !act_scale) return BITLINEAR_ERR_NULL;
+  if (!aligned16(x_bf16) || !aligned16(x_q) || !aligned16(act_scale) || (x_ops && !aligned16(x_ops)))
+    return BITLINEAR_ERR_ALIGN;
+  if (!workspace || workspace_bytes < bitlinear_quant_act_per_tensor_workspace_bytes(M))
+    return BITLINEAR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return BITLINEAR_ERR_ALIGN;
+  const DeviceState* dev = current_device();
+  if (!dev) return BITLINEAR_ERR_DEVICE;
+  return from_cuda(launch_quant_act_per_tensor(static_cast<const uint16_t*>(x_bf16), M, K, x_q, act_scale,
+                                               static_cast<uint8_t*>(x_ops), static_cast<float*>(workspace),
+                                               (flags & BITLINEAR_FLAG_PDL) != 0,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 1 || K < 1) return 0;
   return forward_workspace_bytes(M, N, K);

@@ -21,7 +21,7 @@
 // codes (16 inputs) is expanded by byte permutes into int8 words of inputs
 // (0,2,4,6), (8..14 even), (1,3,5,7), (9..15 odd) (code 0 -> 0, 1 -> +1,
 // 2 -> -1); the staged activations are permuted the same way, so a word is four
-// dp4a per token.  The int32 sums are exact (|acc| <= 127 K < 2^31).
+// dp4a per token.  The int32 sums are exact (|acc| <= 128 K < 2^31).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>

@@ -50,6 +50,15 @@ cudaError_t launch_pack_weights(const float* W, int64_t N, int64_t K, float eps,
                                 float* w_scale, float* gamma_out, void* workspace, int* dev_err,
                                 cudaStream_t stream);
 
+// The same packing with one absmean per output row (written to w_scale); no scratch.
+cudaError_t launch_pack_weights_per_channel(const float* W, int64_t N, int64_t K, float eps, uint8_t* packed,
+                                            float* w_scale, int* dev_err, cudaStream_t stream);
+
+// Per-tensor absmax quantization with Q_b = 128 (no RMSNorm): per-row maxima into
+// `row_max` (M floats of scratch), then codes with one scale for all rows.
+cudaError_t launch_quant_act_per_tensor(const uint16_t* x, int64_t M, int64_t K, int8_t* x_q, float* act_scale,
+                                        uint8_t* x_ops, float* row_max, bool pdl, cudaStream_t stream);
+
 // ---- quant_act -----------------------------------------------------------
 // x_ops: optional tensor-core operand planes of the codes (act_ops.cuh), or nullptr.
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,

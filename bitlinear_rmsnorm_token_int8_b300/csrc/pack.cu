@@ -58,10 +58,9 @@ absmean_bins_kernel(const float4* __restrict__ w4, int64_t n4, unsigned long lon
     if (s_bins[i]) atomicAdd(&bins[i], s_bins[i]);
 }
 
-// One thread.  S = sum_e bins[e] * 2^(max(e,1)-1) in units of 2^-149.
-__global__ void gamma_finalize_kernel(const unsigned long long* __restrict__ bins, uint64_t count,
-                                      float eps, float* __restrict__ gd, float* __restrict__ gamma_out) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+// The exact mean S / count rounded once to binary32 (nearest, ties to even), where
+// S = sum_e bins[e] * 2^(max(e,1)-1) in units of 2^-149 (count < 2^32).  One thread.
+__device__ float exact_mean_f32(const unsigned long long* bins, uint64_t count) {
   constexpr int L = 16;                      // 512 bits: S < 2^342, then shifted by 64
   uint32_t s[L];
 #pragma unroll
@@ -111,18 +110,61 @@ __global__ void gamma_finalize_kernel(const unsigned long long* __restrict__ bin
     if (bits >= 0x7f800000u) bits = 0x7f800000u;
     gamma = __uint_as_float(bits);
   }
+  return gamma;
+}
+
+// One thread: gamma of the whole matrix and d = fl32(gamma + eps).
+__global__ void gamma_finalize_kernel(const unsigned long long* __restrict__ bins, uint64_t count,
+                                      float eps, float* __restrict__ gd, float* __restrict__ gamma_out) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const float gamma = exact_mean_f32(bins, count);
   gd[0] = gamma;
   gd[1] = __fadd_rn(gamma, eps);
   if (gamma_out) *gamma_out = gamma;
 }
 
+// Per output channel: CTA n sums |W[n, :]| into exponent bins in shared memory
+// (order free, as absmean_bins_kernel) and its thread 0 writes gamma_n, the exact
+// row mean rounded once, to w_scale[n].  Rows n = blockIdx.x, blockIdx.x + gridDim.x, ...
+__global__ void __launch_bounds__(kBinsThreads)
+row_absmean_kernel(const float4* __restrict__ w4, int64_t N, int64_t K4, float* __restrict__ w_scale,
+                   int* __restrict__ dev_err) {
+  __shared__ unsigned long long s_bins[256];
+  for (int64_t n = blockIdx.x; n < N; n += gridDim.x) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) s_bins[i] = 0ull;
+    __syncthreads();
+    bool bad = false;
+    for (int64_t i = threadIdx.x; i < K4; i += blockDim.x) {
+      const float4 v = __ldg(w4 + n * K4 + i);
+      const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t bits = __float_as_uint(f[j]) & 0x7fffffffu;
+        const uint32_t e = bits >> 23;
+        uint32_t mant = bits & 0x7fffffu;
+        if (e == 255u) { bad = true; continue; }
+        if (bits == 0u) continue;
+        if (e != 0u) mant |= 0x800000u;
+        atomicAdd(&s_bins[e], (unsigned long long)mant);
+      }
+    }
+    if (bad) atomicCAS(dev_err, 0, kDevErrNonFinite);
+    __syncthreads();
+    if (threadIdx.x == 0) w_scale[n] = exact_mean_f32(s_bins, (uint64_t)(K4 * 4));
+    __syncthreads();                          // thread 0 has read the bins before the next row clears them
+  }
+}
+
 // One thread per 16-byte chunk of the tiled layout (64 weights of one row; see
-// internal.h): codes of rows >= N or k >= K are 0.
+// internal.h): codes of rows >= N or k >= K are 0.  One scale for the matrix (gd =
+// gamma, fl32(gamma + eps); gamma is written to every w_scale[n]), or, with per_row,
+// the row's own gamma_n read from w_scale[n] and d = fl32(gamma_n + eps).
 __global__ void ternarize_pack_kernel(const float* __restrict__ W, int64_t N, int64_t K,
                                       int64_t nseg, int64_t chunks, int64_t Np, const float* __restrict__ gd,
-                                      uint8_t* __restrict__ packed, float* __restrict__ w_scale) {
-  const float gamma = gd[0];
-  const float d = gd[1];
+                                      uint8_t* __restrict__ packed, float* __restrict__ w_scale, float eps,
+                                      bool per_row) {
+  const float gamma = per_row ? 0.0f : gd[0];
+  float d = per_row ? 0.0f : gd[1];
   const int64_t full_tiles = Np / 128, tile_chunks = nseg * 128 * 8;   // chunks of a full tile
   for (int64_t ci = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; ci < chunks;
        ci += (int64_t)gridDim.x * blockDim.x) {
@@ -137,6 +179,7 @@ __global__ void ternarize_pack_kernel(const float* __restrict__ W, int64_t N, in
     const int64_t k0 = seg * 512 + c * 64;
     uint32_t out[4] = {0u, 0u, 0u, 0u};
     if (n < N) {
+      if (per_row) d = __fadd_rn(w_scale[n], eps);
       const float* wr = W + n * K;
 #pragma unroll 4
       for (int q = 0; q < 16; ++q) {             // 16 groups of four weights = 16 bytes
@@ -154,7 +197,7 @@ __global__ void ternarize_pack_kernel(const float* __restrict__ W, int64_t N, in
           out[q >> 2] |= byte << (8 * (q & 3));
         }
       }
-      if (seg == 0 && c == 0) w_scale[n] = gamma;
+      if (seg == 0 && c == 0 && !per_row) w_scale[n] = gamma;
     }
     *reinterpret_cast<uint4*>(packed + (ci << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
   }
@@ -183,8 +226,25 @@ cudaError_t launch_pack_weights(const float* W, int64_t N, int64_t K, float eps,
   int64_t pblocks = (chunks + 255) / 256;
   if (pblocks > (int64_t)sms * 16) pblocks = (int64_t)sms * 16;
   ternarize_pack_kernel<<<(unsigned)pblocks, 256, 0, stream>>>(W, N, K, nseg, chunks, packed_rows(N), gd, packed,
-                                                               w_scale);
+                                                               w_scale, eps, false);
   count_launches(3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weights_per_channel(const float* W, int64_t N, int64_t K, float eps, uint8_t* packed,
+                                            float* w_scale, int* dev_err, cudaStream_t stream) {
+  const int sms = num_sms();
+  const int64_t rblocks = N < (int64_t)sms * 8 ? N : (int64_t)sms * 8;
+  row_absmean_kernel<<<(unsigned)rblocks, kBinsThreads, 0, stream>>>(reinterpret_cast<const float4*>(W), N, K / 4,
+                                                                      w_scale, dev_err);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int64_t chunks = packed_layout_bytes(N, K) / 16;
+  int64_t pblocks = (chunks + 255) / 256;
+  if (pblocks > (int64_t)sms * 16) pblocks = (int64_t)sms * 16;
+  ternarize_pack_kernel<<<(unsigned)pblocks, 256, 0, stream>>>(W, N, K, packed_nseg(K), chunks, packed_rows(N),
+                                                               nullptr, packed, w_scale, eps, true);
+  count_launches(2);
   return cudaGetLastError();
 }
 

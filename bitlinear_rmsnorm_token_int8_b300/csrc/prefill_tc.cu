@@ -8,8 +8,9 @@
 // The method's integer contraction is a dense matmul once M is large, so it is
 // run as one: this GPU has no int8 tcgen05 MMA, so each int8 code enters as two
 // exact e4m3 values (16 h' + l', act_ops.cuh) against e4m3 weights of -1/0/+1,
-// two MMAs per k step into one fp32 accumulator, exact while |acc| < 2^24
-// (|acc| <= 127 K <= 2^23).
+// two MMAs per k step into one fp32 accumulator, exact while every partial sum
+// stays below 2^24 in magnitude (at most 128 K + 8 K <= 2^23 + 2^19 for codes
+// in [-128, 127] and K <= 65536).
 //
 // Tile: 128 weight rows (MMA M, operand A) x TT = 256 or 128 tokens (MMA N,
 // operand B), persistent clusters of CL = 1 or 2 CTAs over tiles (TMA multicast

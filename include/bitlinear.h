@@ -167,6 +167,24 @@ bitlinear_status bitlinear_pack_weights_static(const float *W, int64_t N, int64_
                                                uint8_t *packed, float *w_scale, float *gamma_out,
                                                void *stream);
 
+/*
+ * Ternarization with a scale per output channel ([P2-wr] "BitNet-2B-4T:
+ * Inside the 2B-Parameter, 4T-Token 1-Bit LLM", section "Weight
+ * Representation: Ternary + Scale, Not Pure Binary": W_bit x s, s in R^d):
+ * the absmean of [P4-eq] item 1 taken over each row,
+ *
+ *   gamma_n  = (1/K) sum_k |W[n][k]|, the exact row mean rounded once to binary32
+ *   W_q[n]   = Clip(Round(W[n] / fl32(gamma_n + eps)), -1, 1)
+ *
+ * and w_scale[n] = gamma_n, which bitlinear_forward applies per output row.
+ * (The page stores s in FP16; w_scale stays binary32 here.)
+ * W, N, K, eps, packed, device errors: as bitlinear_pack_weights.
+ * w_scale  [N] fp32 out: gamma_n.
+ * Needs no scratch.
+ */
+bitlinear_status bitlinear_pack_weights_per_channel(const float *W, int64_t N, int64_t K, float eps,
+                                                    uint8_t *packed, float *w_scale, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* 2. activations                                                            */
 /* ------------------------------------------------------------------------ */
@@ -214,6 +232,31 @@ bitlinear_status bitlinear_quant_act(const void *x_bf16, const void *gain_bf16, 
                                      int64_t M, int64_t K, int8_t *x_q, float *act_scale,
                                      void *x_ops, unsigned flags, void *stream);
 
+/* Bytes of scratch that bitlinear_quant_act_per_tensor needs (4 M, rounded up). */
+size_t bitlinear_quant_act_per_tensor_workspace_bytes(int64_t M);
+
+/*
+ * Per-tensor absmax quantization with Q_b = 128 ([P5-aq] "BitNet 1-bit LLM
+ * Inference Framework", BitLinear.activation_quantize), the scale-granularity
+ * variant of bitlinear_quant_act: one scale for all M x K values and no RMSNorm,
+ *
+ *   gamma    = max_{t,k} |x[t][k]|
+ *   x_q[t,k] = Round(Clip(fl32(fl32(x * 128) / fl32(gamma + 1e-8)), -128, 127))
+ *   act_scale[t] = gamma / 128                     (the same for every token)
+ *
+ * The clip comes before the rounding, as in the page's code, so codes span
+ * [-128, 127]; the quotient is rounded once to binary32 before Round (ties to
+ * even), so the codes are exact given that quotient.  bitlinear_forward accepts
+ * these codes and scales unchanged (y = acc * gamma / 128 * w_scale).
+ *
+ * x_bf16, M, K, x_q, act_scale, x_ops, flags: as bitlinear_quant_act.
+ * workspace >= bitlinear_quant_act_per_tensor_workspace_bytes(M) bytes of device
+ *           scratch (the row maxima); contents on entry do not matter.
+ */
+bitlinear_status bitlinear_quant_act_per_tensor(const void *x_bf16, int64_t M, int64_t K, int8_t *x_q,
+                                                float *act_scale, void *x_ops, void *workspace,
+                                                size_t workspace_bytes, unsigned flags, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* 3. ternary contraction + dequantization                                   */
 /* ------------------------------------------------------------------------ */
@@ -232,7 +275,8 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   y[t][n]   = fl32(fl32(acc * act_scale[t]) * w_scale[n]) then, for bf16
  *               output, rounded to nearest even bf16.
  *
- * x_q       [M,K] int8 (from bitlinear_quant_act).  Codes must lie in [-127,127].
+ * x_q       [M,K] int8 (from bitlinear_quant_act or bitlinear_quant_act_per_tensor).
+ *           Codes may be any int8 in [-128, 127].
  *           May be NULL when x_ops is given.
  * act_scale [M] fp32.
  * x_ops     the same codes in operand form (bitlinear_quant_act's x_ops), or NULL.
@@ -261,7 +305,7 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *
  * Exactness: every route forms acc as the exact integer sum.  With x_q given and
  * M <= BITLINEAR_CODES_MAX_M (see there for the exact shape rule) a CUDA-core
- * kernel contracts the int8 codes with int32 dot products (|acc| <= 127 K < 2^31).
+ * kernel contracts the int8 codes with int32 dot products (|acc| <= 128 K < 2^31).
  * Otherwise the tensor cores contract e4m3 operands: each code enters as two
  * exact e4m3 values (see bitlinear_act_ops_bytes) and every fp32 accumulator
  * stays an integer below 2^24 in magnitude (at most 128 K <= 2^23).  Both give

@@ -245,3 +245,26 @@ def test_packed_layout_swizzle_example():
 def _lib_bytes(N, K):
     blbuild.build()
     return bl.lib().bitlinear_packed_bytes(N, K)
+
+
+def test_scale_variant_argument_errors(L):
+    pc = L.bitlinear_pack_weights_per_channel
+    assert pc(None, 8, 8, 1e-5, FAKE, FAKE, None) == ERR_NULL
+    assert pc(FAKE, 8, 6, 1e-5, FAKE, FAKE, None) == ERR_SHAPE
+    assert pc(FAKE, 8, 8, -1.0, FAKE, FAKE, None) == ERR_SHAPE
+    assert pc(FAKE, 1 << 20, 1 << 12, 1e-5, FAKE, FAKE, None) == ERR_SHAPE
+    assert pc(FAKE, 8, 8, 1e-5, FAKE + 4, FAKE, None) == ERR_ALIGN
+    need = L.bitlinear_quant_act_per_tensor_workspace_bytes(100)
+    assert need >= 400 and need % 256 == 0
+    qt = L.bitlinear_quant_act_per_tensor
+    assert qt(None, 4, 256, FAKE, FAKE, None, FAKE, need, 0, None) == ERR_NULL
+    assert qt(FAKE, 4, 256, None, FAKE, None, FAKE, need, 0, None) == ERR_NULL
+    assert qt(FAKE, 4, 12, FAKE, FAKE, None, FAKE, need, 0, None) == ERR_SHAPE
+    assert qt(FAKE, 0, 256, None, None, None, None, 0, 0, None) == OK       # empty: nothing to touch
+    assert qt(FAKE, 4, 256, FAKE, FAKE, None, None, 0, 0, None) == ERR_WS
+    assert qt(FAKE, 4, 256, FAKE, FAKE, FAKE + 8, FAKE, need, 0, None) == ERR_ALIGN
+    assert qt(FAKE, 4, 256, FAKE, FAKE, None, FAKE, need, 2, None) == ERR_FLAGS
+    import torch
+    if not torch.cuda.is_available():
+        assert pc(FAKE, 8, 8, 1e-5, FAKE, FAKE, None) == ERR_DEVICE
+        assert qt(FAKE, 4, 256, FAKE, FAKE, None, FAKE, need, 1, None) == ERR_DEVICE
