@@ -29,6 +29,7 @@ __all__ = [
     "bitlinear_forward_workspace_bytes", "bitlinear_pack_workspace_bytes", "OUT_F32", "OUT_BF16",
     "STATUS", "bitlinear_kernel_launches", "bitlinear_act_ops_bytes", "FLAG_PDL", "OUT_BF16_ADD",
     "bitlinear_block_forward", "bitlinear_block_workspace_bytes", "pack_stacked", "LAYER_FIELDS",
+    "bitlinear_block_trace_bytes", "block_trace_views",
     "bitlinear_linear_forward", "bitlinear_linear_workspace_bytes", "CODES_MAX_M", "bitlinear_linear_route",
     "ROUTE_FUSED", "ROUTE_CODES", "ROUTE_DECODE", "ROUTE_PREFILL", "bitlinear_prefill_cluster_size",
     "bitlinear_pack_weights_per_channel", "bitlinear_quant_act_per_tensor",
@@ -96,7 +97,9 @@ def lib() -> ctypes.CDLL:
         L.bitlinear_get_device_error.restype = I
         L.bitlinear_block_workspace_bytes.argtypes = [I64, I64, I64, I64]
         L.bitlinear_block_workspace_bytes.restype = SZ
-        L.bitlinear_block_forward.argtypes = [P, I, I64, I64, I64, F, P, I64, P, SZ, U, P]
+        L.bitlinear_block_trace_bytes.argtypes = [I64, I64, I64, I64]
+        L.bitlinear_block_trace_bytes.restype = SZ
+        L.bitlinear_block_forward.argtypes = [P, I, I64, I64, I64, F, P, I64, P, SZ, P, SZ, U, P]
         L.bitlinear_block_forward.restype = I
         L.bitlinear_linear_workspace_bytes.argtypes = [I64, I64, I64]
         L.bitlinear_linear_workspace_bytes.restype = SZ
@@ -382,12 +385,43 @@ def bitlinear_block_workspace_bytes(M: int, H: int, NQKV: int, F: int) -> int:
     return int(lib().bitlinear_block_workspace_bytes(M, H, NQKV, F))
 
 
+def bitlinear_block_trace_bytes(M: int, H: int, NQKV: int, F: int) -> int:
+    return int(lib().bitlinear_block_trace_bytes(M, H, NQKV, F))
+
+
+def block_trace_views(trace: torch.Tensor, layer: int, M: int, H: int, NQKV: int, F: int) -> dict:
+    """Views of one layer's part of a bitlinear_block_forward trace (the layout that
+    bitlinear_block_trace_bytes documents): xq_{qkv,o,gate_up,down} int8,
+    sc_{...} fp32, qkv bf16, x_mid bf16, gate_up fp32, x_out bf16."""
+    stride = bitlinear_block_trace_bytes(M, H, NQKV, F)
+    base = trace[layer * stride:(layer + 1) * stride]
+    out, off = {}, 0
+
+    def take(name, nbytes, dtype, shape):
+        nonlocal off
+        out[name] = base[off:off + nbytes].view(dtype).view(*shape)
+        off = (off + nbytes + 255) // 256 * 256
+
+    for name, k in (("qkv", H), ("o", H), ("gate_up", H), ("down", F)):
+        take("xq_" + name, M * k, torch.int8, (M, k))
+    for name in ("qkv", "o", "gate_up", "down"):
+        take("sc_" + name, 4 * M, torch.float32, (M,))
+    take("qkv", 2 * M * NQKV, torch.bfloat16, (M, NQKV))
+    take("x_mid", 2 * M * H, torch.bfloat16, (M, H))
+    take("gate_up", 8 * M * F, torch.float32, (M, 2 * F))
+    take("x_out", 2 * M * H, torch.bfloat16, (M, H))
+    return out
+
+
 def bitlinear_block_forward(layers, x: torch.Tensor, H: int, NQKV: int, F: int, rms_eps: float = 1e-5,
-                            workspace=None, flags: int = 0, stream=None):
+                            workspace=None, flags: int = 0, stream=None, trace=None):
     """The BitLinear stack of len(layers) transformer layers on x [M, H] bf16 (CUDA), in place.
 
     ``layers``: dicts with the CUDA tensors named in :data:`LAYER_FIELDS` (packed weights,
-    fp32 per-row scales, bf16 RMSNorm gains).  Returns x.
+    fp32 per-row scales, bf16 RMSNorm gains).  ``trace``: None, or a uint8 CUDA tensor of
+    len(layers) * :func:`bitlinear_block_trace_bytes` bytes (256-byte aligned) that
+    receives every layer's intermediates (read them with :func:`block_trace_views`).
+    Returns x.
     """
     _cuda(x, "x", torch.bfloat16)
     M = x.shape[0]
@@ -400,9 +434,12 @@ def bitlinear_block_forward(layers, x: torch.Tensor, H: int, NQKV: int, F: int, 
     if workspace is None:
         workspace = torch.empty(bitlinear_block_workspace_bytes(M, H, NQKV, F) + 256, dtype=torch.uint8,
                                 device=x.device)
+    if trace is not None:
+        _cuda(trace, "trace", torch.uint8)
     _check("bitlinear_block_forward", lib().bitlinear_block_forward(
         ctypes.cast(arr, ctypes.c_void_p), len(layers), H, NQKV, F, float(rms_eps), _ptr(x), M,
-        _ptr(workspace), workspace.numel(), int(flags), _stream(stream)))
+        _ptr(workspace), workspace.numel(), _ptr(trace), 0 if trace is None else trace.numel(), int(flags),
+        _stream(stream)))
     return x
 
 

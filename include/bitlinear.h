@@ -410,6 +410,16 @@ typedef struct bitlinear_layer {
 size_t bitlinear_block_workspace_bytes(int64_t M, int64_t H, int64_t NQKV, int64_t F);
 
 /*
+ * Bytes of one layer's trace of bitlinear_block_forward (see its `trace`
+ * argument).  The layer's trace holds, each part starting 256-byte aligned, in
+ * this order: the int8 codes of the inputs of its four BitLinears (qkv, o,
+ * gate_up: [M, H]; down: [M, F]), their token scales ([4][M] fp32), qkv
+ * ([M, NQKV] bf16), x after the O residual ([M, H] bf16), gate|up ([M, 2F]
+ * fp32) and x after the down residual ([M, H] bf16).
+ */
+size_t bitlinear_block_trace_bytes(int64_t M, int64_t H, int64_t NQKV, int64_t F);
+
+/*
  * The BitLinear projections of n_layers transformer layers on M tokens, with
  * x [M, H] bf16 (device) as the residual stream, updated in place.  Per layer
  * (every "BitLinear" = RMSNorm + int8 quantization + ternary contraction +
@@ -438,13 +448,20 @@ size_t bitlinear_block_workspace_bytes(int64_t M, int64_t H, int64_t NQKV, int64
  * M         tokens, 1 <= M <= 2^20.
  * workspace >= bitlinear_block_workspace_bytes(M, H, NQKV, F) bytes of device
  *           scratch, 256-byte aligned; contents on entry do not matter.
+ * trace     NULL, or n_layers * bitlinear_block_trace_bytes(M, H, NQKV, F) bytes
+ *           (trace_bytes) of device memory, 256-byte aligned, that receives
+ *           every layer's intermediates (layout at bitlinear_block_trace_bytes)
+ *           for checking each BitLinear on its exact input.  Tracing adds four
+ *           small copy kernels per layer; the results are the same.
  * flags     0 or BITLINEAR_FLAG_PDL (applies to the first kernel; the
  *           following ones always overlap with their predecessor).
+ * Every contraction pulls the packed weights of the projection after it into L2
+ * (see the l2_prefetch argument of bitlinear_forward).
  */
 bitlinear_status bitlinear_block_forward(const bitlinear_layer *layers, int n_layers, int64_t H,
                                          int64_t NQKV, int64_t F, float rms_eps, void *x_bf16,
                                          int64_t M, void *workspace, size_t workspace_bytes,
-                                         unsigned flags, void *stream);
+                                         void *trace, size_t trace_bytes, unsigned flags, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* device error word                                                         */
