@@ -553,7 +553,7 @@ def measure_decode(bl, synth, torch, dev, workload, layers, steps, warmup, e2e=T
     return out
 
 
-def measure_prefill(bl, synth, torch, dev, steps, warmup):
+def measure_prefill(bl, synth, torch, dev, steps, warmup, peaks=None):
     """M = 2048 prefill of the 8B-class shapes (4096->14336, 14336->4096): per shape one
     graph of the whole BitLinear layer (bitlinear_linear_forward: RMSNorm + quantization
     into the operand form, then the contraction); CUDA events around `steps` replays.
@@ -609,17 +609,54 @@ def measure_prefill(bl, synth, torch, dev, steps, warmup):
         tot_ms += ms["pair"]
         tot_fwd_ms += ms["fwd"]
         del packed, w_scale, x, ops, ws, y, graphs
-    _, bf16_tf, src = measured_peaks()
-    fp8_peak = 2.0 * bf16_tf          # e4m3 dense rate = 2x bf16 (nominal ratio)
     method_tops = tot_ops / (tot_fwd_ms * 1e9)
-    out.update({"int8_equiv_tops": tot_ops / (tot_ms * 1e9), "fwd_int8_equiv_tops": method_tops,
+    layer_tops = tot_ops / (tot_ms * 1e9)
+    pk = peaks or {}
+    if "tcgen05_e4m3_tflops" in pk:
+        fp8_peak, src = pk["tcgen05_e4m3_tflops"], "measured (tcgen05 kind::f8f6f4 m128n256k32 microbenchmark)"
+    else:
+        _, bf16_tf, s = measured_peaks()
+        fp8_peak, src = 2.0 * bf16_tf, f"{s} bf16 cuBLAS x 2 (nominal e4m3:bf16 ratio)"
+    out.update({"int8_equiv_tops": layer_tops, "fwd_int8_equiv_tops": method_tops,
                 "roofline": {"bound": "tensor", "achieved": method_tops,
                              "unit": "TFLOP/s (int8-equivalent method work, 2 M N K)",
                              "peak": fp8_peak, "frac": method_tops / fp8_peak,
                              "mma_pipe_frac": 2.0 * method_tops / fp8_peak,
-                             "layer_frac": (tot_ops / (tot_ms * 1e9)) / fp8_peak,
+                             "layer_frac": layer_tops / fp8_peak,
                              "kernel": "prefill_tc_kernel (tcgen05 kind::f8f6f4, two e4m3 MMAs per int8 product)",
-                             "peak_source": f"{src} bf16 cuBLAS x 2 (nominal e4m3:bf16 ratio)"}})
+                             "peak_source": src}})
+    if "mma_sync_s8_tops" in pk:
+        out["vs_int8_mma_sync"] = {"peak_tops": pk["mma_sync_s8_tops"],
+                                   "ratio": method_tops / pk["mma_sync_s8_tops"],
+                                   "note": "the only int8 tensor-core MMA on this GPU (tcgen05 kind::i8 is "
+                                           "rejected for sm_103a)"}
+    return out
+
+
+def measure_mma_peaks(torch, dev):
+    """Dense MMA rates from libbitlinear_probe.so (back-to-back MMAs on on-chip
+    operands, one CTA per SM for tcgen05), by CUDA events, with the SM clock seen."""
+    import ctypes
+    path = os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "libbitlinear_probe.so")
+    if not os.path.exists(path):
+        return None
+    L = ctypes.CDLL(path)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ms = ctypes.c_float()
+    out = {}
+    with ClockSampler(dev.index or 0) as clk:
+        for kind, key, flop in ((0, "tcgen05_e4m3_tflops", 2 * 128 * 256 * 32),
+                                (1, "tcgen05_bf16_tflops", 2 * 128 * 256 * 16)):
+            iters = 16384
+            if L.bitlinear_probe_tcgen05(kind, iters, sms, ctypes.byref(ms)) == 0:
+                out[key] = flop * iters * sms / (ms.value * 1e-3) / 1e12
+        for kind, key in ((0, "mma_sync_s8_tops"), (1, "mma_sync_e4m3_tflops")):
+            iters, ctas = 2048, sms * 8
+            if L.bitlinear_probe_mma_sync(kind, iters, ctas, ctypes.byref(ms)) == 0:
+                out[key] = 2 * 16 * 8 * 32 * 8 * iters * ctas * 8 / (ms.value * 1e-3) / 1e12
+    out["clocks"] = clk.summary()
+    out["how"] = ("tcgen05: m128n256 MMAs, A in tensor memory, B in shared memory, 16384 per CTA on one CTA per "
+                  "SM; mma.sync: m16n8k32, 8 warps x 8 independent accumulators, 8 CTAs per SM")
     return out
 
 
@@ -695,7 +732,9 @@ def our_arm(args):
         extra["decode_2b"]["roofline"] = {k: d2["roofline"][k] for k in ("achieved", "frac", "avg_launch_us",
                                                                          "per_shape")}
         torch.cuda.empty_cache()
-        extra["prefill"] = measure_prefill(bl, synth, torch, dev, max(3, args.steps), args.warmup)
+        extra["mma_peaks"] = measure_mma_peaks(torch, dev)
+        extra["prefill"] = measure_prefill(bl, synth, torch, dev, max(3, args.steps), args.warmup,
+                                           peaks=extra["mma_peaks"])
         torch.cuda.empty_cache()
         extra["stack_2b"] = measure_stack(bl, synth, torch, dev, LAYERS["stack_2b"], max(3, args.steps // 2),
                                           args.warmup)
