@@ -63,13 +63,13 @@ cudaError_t launch_quant_act_per_tensor(const uint16_t* x, int64_t M, int64_t K,
 // x_ops: optional tensor-core operand planes of the codes (act_ops.cuh), or nullptr.
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,
                              int64_t K, int8_t* x_q, float* act_scale, uint8_t* x_ops, bool pdl,
-                             cudaStream_t stream, L2Prefetch pf = {});
+                             cudaStream_t stream);
 
 // Same with a row pitch `ld` (elements, a multiple of 8) or, if `glu` is set, the
 // ReLU^2-gated rows of fp32 [gate | up] (x unused).  x_q may be null.
 cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu, const uint16_t* gain,
                                 float rms_eps, int64_t M, int64_t K, int8_t* x_q, float* act_scale,
-                                uint8_t* x_ops, bool pdl, cudaStream_t stream, L2Prefetch pf = {});
+                                uint8_t* x_ops, bool pdl, cudaStream_t stream);
 
 // ---- activation operands ---------------------------------------------------
 size_t act_ops_bytes(int64_t M, int64_t K);

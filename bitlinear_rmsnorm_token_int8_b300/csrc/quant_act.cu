@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(1024)
 quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restrict__ glu,
                  const uint4* __restrict__ gain, float rms_eps,
                  int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale,
-                 uint8_t* __restrict__ x_ops, int64_t M, const uint8_t* pf, uint64_t pf_bytes) {
+                 uint8_t* __restrict__ x_ops, int64_t M) {
   const int V = K >> 3;                      // 16-byte vectors per row
   const int U = (V + 1) >> 1;                // units of 16 inputs
   const int row = blockIdx.x;
@@ -105,9 +105,6 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
       if (u < U && (u & 3) == 0) prefetch_l2(xr + 2 * u);   // one per 128-byte line
     }
   }
-  // the caller's L2 prefetch (the weights of the contraction that follows), spread
-  // over the first warp
-  if (tid < 32) l2_prefetch_share(pf, pf_bytes, tid, 32);
   // Let the next kernel launch now: it waits for this one to complete, and this one
   // completes only after the kernel before it (the wait below), so the next kernel
   // can set up and prefetch its weights while the previous one still runs.
@@ -202,7 +199,7 @@ constexpr uint32_t kRowsSpin = 1u << 24;
 __global__ void __launch_bounds__(kRowsThreads, 2)
 quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __restrict__ gain, float rms_eps,
                   int K, int8_t* __restrict__ x_q, float* __restrict__ act_scale, uint8_t* __restrict__ x_ops,
-                  int64_t M, int* dev_err, const uint8_t* pf, uint64_t pf_bytes) {
+                  int64_t M, int* dev_err) {
   extern __shared__ __align__(16) uint8_t qsm[];
   const int rb = K * 2;                            // bytes of a row (a multiple of 16)
   const uint32_t buf0 = smem_u32(qsm), gbuf = buf0 + 2 * rb;
@@ -224,7 +221,6 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __
   for (int v = tid; v < V; v += kRowsThreads)
     *reinterpret_cast<uint4*>(qsm + 2 * rb + 16 * v) =
         gain ? __ldg(reinterpret_cast<const uint4*>(gain) + v) : kOnes;
-  if (tid < 32) l2_prefetch_share(pf, pf_bytes, tid, 32);
   __syncthreads();
   pdl_launch_dependents();                         // as in quant_act_kernel
   pdl_wait();                                      // x may be the previous kernel's output
@@ -347,13 +343,13 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __
 
 cudaError_t launch_quant_act(const uint16_t* x, const uint16_t* gain, float rms_eps, int64_t M,
                              int64_t K, int8_t* x_q, float* act_scale, uint8_t* x_ops, bool pdl,
-                             cudaStream_t stream, L2Prefetch pf) {
-  return launch_quant_act_ex(x, K, nullptr, gain, rms_eps, M, K, x_q, act_scale, x_ops, pdl, stream, pf);
+                             cudaStream_t stream) {
+  return launch_quant_act_ex(x, K, nullptr, gain, rms_eps, M, K, x_q, act_scale, x_ops, pdl, stream);
 }
 
 cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu, const uint16_t* gain,
                                 float rms_eps, int64_t M, int64_t K, int8_t* x_q, float* act_scale,
-                                uint8_t* x_ops, bool pdl, cudaStream_t stream, L2Prefetch pf) {
+                                uint8_t* x_ops, bool pdl, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
   const int sms = num_sms();
   // Many long rows of bf16 input: persistent CTAs that stream rows through shared
@@ -381,7 +377,7 @@ cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu,
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     cudaError_t e = cudaLaunchKernelEx(&cfg, quant_rows_kernel, x, ld, gain, rms_eps, (int)K, x_q, act_scale,
-                                       x_ops, M, dev_err, pf.p, pf.bytes);
+                                       x_ops, M, dev_err);
     count_launches(1);
     return e;
   }
@@ -414,10 +410,10 @@ cudaError_t launch_quant_act_ex(const uint16_t* x, int64_t ld, const float* glu,
   const uint4* gv = reinterpret_cast<const uint4*>(gain);
   cudaError_t e;
   switch (tv) {
-    case 1: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<1>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M, pf.p, pf.bytes); break;
-    case 2: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M, pf.p, pf.bytes); break;
-    case 4: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<4>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M, pf.p, pf.bytes); break;
-    default: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<8>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M, pf.p, pf.bytes); break;
+    case 1: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<1>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<2>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<4>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
+    default: e = cudaLaunchKernelEx(&cfg, quant_act_kernel<8>, xv, (int64_t)(ld / 8), glu, gv, rms_eps, (int)K, x_q, act_scale, x_ops, M); break;
   }
   count_launches(1);
   return e;

@@ -94,10 +94,12 @@ def test_quant_act_matches_oracle(M, K, gain, rms, outliers):
     assert np.all(np.abs(sc - osig) <= SIGMA_RTOL * osig)
 
 
-@pytest.mark.parametrize("M,K,gain,rms", [(600, 4104, True, True), (640, 6912, False, True), (700, 8192, True, False)])
+@pytest.mark.parametrize("M,K,gain,rms", [(600, 4104, True, True), (640, 6912, False, True), (700, 8192, True, False),
+                                          (33, 2560, True, True), (2048, 4096, True, True), (300, 14336, False, True),
+                                          (97, 65536, True, True)])
 def test_quant_act_many_rows_matches_oracle(M, K, gain, rms):
-    # M >= 4 x the SM count and K > 4096: persistent CTAs streaming rows through
-    # shared memory; K = 4104 ends in half a 16-input unit
+    # many rows: one CTA per row, or for M >= 4 x the SM count and K > 4096 persistent
+    # CTAs streaming rows through shared memory; K = 4104 ends in half a 16-input unit
     x = synth.activations(M, K, seed=M + 3 * K)
     g = synth.rms_gains(K, seed=K + 1) if gain else None
     eps = RMS_EPS if rms else -1.0
