@@ -285,7 +285,8 @@ def traffic_record(workload, kernel_srcs):
 
 def kernel_sources():
     csrc = os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc")
-    return [os.path.join(csrc, f) for f in ("decode_cc.cu", "quant_math.cuh", "decode_tc.cu", "device_util.cuh")]
+    return [os.path.join(csrc, f) for f in ("decode_cc.cu", "decode_dp4a.cu", "quant_math.cuh", "decode_tc.cu",
+                                            "device_util.cuh")]
 
 
 def timed_replays(torch, graph, stream, steps):
@@ -300,7 +301,8 @@ def timed_replays(torch, graph, stream, steps):
     return e0.elapsed_time(e1) / steps
 
 
-def measure_decode(bl, synth, torch, dev, workload, layers, steps, warmup, e2e=True, clocks=True):
+def measure_decode(bl, synth, torch, dev, workload, layers, steps, warmup, e2e=True, clocks=True,
+                   min_warmup_s=1.0):
     """The decode step of `workload` (see the module docstring) as one CUDA graph:
     value, step time, per-shape launch times and roofline, and the end-to-end pass."""
     wl = synth.WORKLOADS[workload]
@@ -382,7 +384,7 @@ def measure_decode(bl, synth, torch, dev, workload, layers, steps, warmup, e2e=T
     # ---- warmup: W replays, then more until ~1 s has passed (clock ramp-up)
     t0 = time.perf_counter()
     n = 0
-    while n < warmup or time.perf_counter() - t0 < 1.0:
+    while n < warmup or time.perf_counter() - t0 < min_warmup_s:
         graph.replay()
         n += 1
         if n % 20 == 0:
@@ -722,7 +724,7 @@ def our_arm(args):
         return 0
 
     head = measure_decode(bl, synth, torch, dev, workload, args.layers or LAYERS[workload], args.steps,
-                          args.warmup, e2e=True, clocks=True)
+                          args.warmup, e2e=True, clocks=True, min_warmup_s=args.min_warmup_s)
     extra = {}
     if workload == HEADLINE and not args.headline_only:
         d2 = measure_decode(bl, synth, torch, dev, "decode_2b", LAYERS["decode_2b"], args.steps, args.warmup,
@@ -781,6 +783,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="layers of the workload (default: its own)")
     ap.add_argument("--ref-seconds", type=float, default=12.0, help="CPU oracle seconds per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="warm-up replays continue at least this long (clock ramp-up; 0 under a profiler)")
     ap.add_argument("--headline-only", action="store_true",
                     help="only the headline decode (no decode_2b, prefill or stack_2b objects)")
     ap.add_argument("--workload", choices=["decode_8b", "decode_2b", "stack_2b"], default=HEADLINE)
