@@ -35,7 +35,6 @@
 // they are.  Size: 2 * Mp * Kp bytes.
 #pragma once
 
-#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace bitlinear {
@@ -49,34 +48,45 @@ __host__ __device__ __forceinline__ int64_t act_ops_kpad(int64_t K) {
   return (K + kOpsBlockK - 1) / kOpsBlockK * kOpsBlockK;
 }
 
-__device__ __forceinline__ uint32_t e4m3_exact(int v) {
-  return (uint32_t)__nv_cvt_float_to_fp8((float)v, __NV_SATFINITE, __NV_E4M3);
-}
-
 __host__ __device__ __forceinline__ int64_t act_ops_mt(int64_t M) { return (M + 7) / 8 * 8; }
 
-// Four words of e4m3 bytes of 16 consecutive codes in the pi order, for each plane.
-__device__ __forceinline__ void act_ops_words(const int (&q)[16], uint32_t (&H)[4], uint32_t (&L)[4]) {
+// Two small integers exact in e4m3 as two bytes, `lo` in the low byte (the PTX
+// cvt to e4m3x2 puts its first source operand in the upper byte).  The ints
+// become floats by the 1.5 * 2^23 offset (two full-rate operations) rather than
+// a conversion instruction.
+__device__ __forceinline__ uint32_t e4m3x2_exact(int lo, int hi) {
+  const float fl = __fsub_rn(__int_as_float(lo + 0x4B400000), 12582912.0f);
+  const float fh = __fsub_rn(__int_as_float(hi + 0x4B400000), 12582912.0f);
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(fh), "f"(fl));
+  return (uint32_t)r;
+}
+
+// Four words of e4m3 bytes of 16 consecutive codes in the pi order, for each
+// plane; the codes come as int8 bytes, code j in byte j % 4 of q[j / 4].
+__device__ __forceinline__ void act_ops_words(const uint32_t (&q)[4], uint32_t (&H)[4], uint32_t (&L)[4]) {
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    H[w] = 0u;
-    L[w] = 0u;
+    int hh[4], ll[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const int pos = 4 * w + b;
-      const int x = q[pos < 8 ? 2 * pos : 2 * (pos - 8) + 1];
+      const int j = pos < 8 ? 2 * pos : 2 * (pos - 8) + 1;
+      const int x = (int)(int8_t)(q[j >> 2] >> (8 * (j & 3)));
       const int h = (x + 8) >> 4;                 // arithmetic shift: floor
-      H[w] |= e4m3_exact(16 * h) << (8 * b);
-      L[w] |= e4m3_exact(x - 16 * h) << (8 * b);
+      hh[b] = 16 * h;
+      ll[b] = x - 16 * h;
     }
+    H[w] = e4m3x2_exact(hh[0], hh[1]) | (e4m3x2_exact(hh[2], hh[3]) << 16);
+    L[w] = e4m3x2_exact(ll[0], ll[1]) | (e4m3x2_exact(ll[2], ll[3]) << 16);
   }
 }
 
-// Writes the operand bytes of 16 consecutive codes q[0..15] = x_q[m][k..k+15]
-// (k a multiple of 16; zero codes for the padding beyond K) in the decode
-// layout: two 16-byte stores, one per plane.
+// Writes the operand bytes of 16 consecutive codes x_q[m][k..k+15], packed as
+// int8 bytes in q (k a multiple of 16; zero codes for the padding beyond K), in
+// the decode layout: two 16-byte stores, one per plane.
 __device__ __forceinline__ void write_act_ops16(uint8_t* __restrict__ ops, int64_t M, int64_t m,
-                                                int64_t k, int64_t Kp, const int (&q)[16]) {
+                                                int64_t k, int64_t Kp, const uint32_t (&q)[4]) {
   uint32_t H[4], L[4];
   act_ops_words(q, H, L);
   const int64_t Mt = act_ops_mt(M);
@@ -97,7 +107,7 @@ __device__ __forceinline__ int64_t prefill_ops_offset(int64_t m, int64_t k, int6
 
 // Prefill-layout counterpart of write_act_ops16.
 __device__ __forceinline__ void write_act_ops16_prefill(uint8_t* __restrict__ ops, int64_t M, int64_t m,
-                                                        int64_t k, int64_t Kp, const int (&q)[16]) {
+                                                        int64_t k, int64_t Kp, const uint32_t (&q)[4]) {
   uint32_t H[4], L[4];
   act_ops_words(q, H, L);
   const int64_t off = prefill_ops_offset(m, k, Kp);
@@ -107,7 +117,7 @@ __device__ __forceinline__ void write_act_ops16_prefill(uint8_t* __restrict__ op
 
 // Writes 16 codes in the layout that bitlinear_forward uses for M tokens.
 __device__ __forceinline__ void write_act_ops16_any(uint8_t* __restrict__ ops, int64_t M, int64_t m,
-                                                    int64_t k, int64_t Kp, const int (&q)[16]) {
+                                                    int64_t k, int64_t Kp, const uint32_t (&q)[4]) {
   if (act_ops_prefill(M)) write_act_ops16_prefill(ops, M, m, k, Kp, q);
   else write_act_ops16(ops, M, m, k, Kp, q);
 }

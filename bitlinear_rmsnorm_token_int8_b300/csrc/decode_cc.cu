@@ -266,17 +266,8 @@ __global__ void __launch_bounds__(kCcThreads, 1) decode_cc_kernel(const DecodeCc
         uint32_t w[4] = {0u, 0u, 0u, 0u};
         if (m < p.M) {
           const RowQuant rq = row_quant(s_m[m], s_sum[m], p.K, p.rms_eps);
-#pragma unroll
-          for (int hv = 0; hv < 2; ++hv) {
-            float xf[8], gf[8];
-            unpack8(xv[m][hv], xf);
-            unpack8(gv[hv], gf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int q = row_code(__fmul_rn(xf[e], gf[e]), rq);
-              w[2 * hv + (e >> 2)] |= (uint32_t)(q & 0xff) << (8 * (e & 3));
-            }
-          }
+          row_codes<16>([&](int e) { return __fmul_rn(bf16_at(xv[m][e >> 3], e & 7), bf16_at(gv[e >> 3], e & 7)); },
+                        rq, w);
           if (tid == 0) {
             s_sigma[m] = rq.sigma;
             if (blockIdx.x == 0 && p.act_scale_out) p.act_scale_out[m] = rq.sigma;

@@ -293,18 +293,8 @@ __global__ void __launch_bounds__(512) linear_dp4a_kernel(const LinearDp4aParams
 
   // codes of this unit (zero past K), staged permuted for the dot products
   if (tid < p.nseg * 32) {
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int hv = 0; hv < 2; ++hv) {
-      float xf[8], gf[8];
-      unpack8(xv[hv], xf);
-      unpack8(gv[hv], gf);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int q = row_code(__fmul_rn(xf[j], gf[j]), rq);
-        w[2 * hv + (j >> 2)] |= (uint32_t)(q & 0xff) << (8 * (j & 3));
-      }
-    }
+    uint32_t w[4];
+    row_codes<16>([&](int j) { return __fmul_rn(bf16_at(xv[j >> 3], j & 7), bf16_at(gv[j >> 3], j & 7)); }, rq, w);
     const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
     const int s = tid >> 5, cc = (tid >> 2) & 7, j = tid & 3;
     *reinterpret_cast<uint4*>(xsm + s * kSegPitch + cc * kChunkPitch + 16 * j) = permute16(codes);

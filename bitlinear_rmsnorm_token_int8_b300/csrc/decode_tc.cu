@@ -395,20 +395,12 @@ __global__ void act_ops_from_codes_kernel(const int8_t* __restrict__ x_q, int64_
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < M * per_row;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t m = idx / per_row, k = (idx - m * per_row) << 4;
-    int q[16];
+    uint32_t q[4];
 #pragma unroll
     for (int hv = 0; hv < 2; ++hv) {
-      if (k + 8 * hv < K) {
-        const uint2 v = *reinterpret_cast<const uint2*>(x_q + m * K + k + 8 * hv);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          q[8 * hv + j] = (int)(int8_t)(v.x >> (8 * j));
-          q[8 * hv + j + 4] = (int)(int8_t)(v.y >> (8 * j));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) q[8 * hv + j] = 0;
-      }
+      const uint2 v = k + 8 * hv < K ? *reinterpret_cast<const uint2*>(x_q + m * K + k + 8 * hv) : make_uint2(0u, 0u);
+      q[2 * hv] = v.x;
+      q[2 * hv + 1] = v.y;
     }
     write_act_ops16_any(ops, M, m, k, Kp, q);
   }

@@ -30,6 +30,7 @@
 // 127 p is exact (at most 16 + 7 significant bits), and one fused multiply-add
 // forms the difference with a single rounding, which cannot change its sign;
 // an exact zero is a tie and goes to the even code.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -157,33 +158,24 @@ quant_act_kernel(const uint4* __restrict__ x, int64_t ld, const float* __restric
   for (int i = 0; i < UPT; ++i) {
     const int u = tid + i * T;
     if (u < U) {
-      int q[16];
+      uint4 gu[2];
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
-        float xf[8], gf[8];
-        unpack8(xv[i][hv], xf);
         const int v = 2 * u + hv;
-        if constexpr (kPreGain) unpack8(gv_[i][hv], gf);
-        else unpack8((gain && v < V) ? __ldg(gain + v) : kOnes, gf);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) q[8 * hv + j] = row_code(__fmul_rn(xf[j], gf[j]), rq);
-        if (v < V && x_q) {
-          uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            w0 |= (uint32_t)(q[8 * hv + j] & 0xff) << (8 * j);
-            w1 |= (uint32_t)(q[8 * hv + j + 4] & 0xff) << (8 * j);
-          }
-          qr[v] = make_uint2(w0, w1);
-        }
+        if constexpr (kPreGain) gu[hv] = gv_[i][hv];
+        else gu[hv] = (gain && v < V) ? __ldg(gain + v) : kOnes;
       }
-      if (x_ops) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, q);   // zero x -> zero code
+      uint32_t w[4];
+      row_codes<16>([&](int j) { return __fmul_rn(bf16_at(xv[i][j >> 3], j & 7), bf16_at(gu[j >> 3], j & 7)); },
+                    rq, w);
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv)
+        if (2 * u + hv < V && x_q) qr[2 * u + hv] = make_uint2(w[2 * hv], w[2 * hv + 1]);
+      if (x_ops) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, w);   // zero x -> zero code
     }
   }
   if (x_ops) {                               // zero operands of the padding up to Kp
-    int z[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) z[j] = 0;
+    const uint32_t z[4] = {0u, 0u, 0u, 0u};
     for (int u = U + tid; u < (int)(Kp >> 4); u += T) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, z);
   }
 }
@@ -306,31 +298,22 @@ quant_rows_kernel(const uint16_t* __restrict__ x, int64_t ld, const uint16_t* __
     // pass 2: codes, the int8 row and the operand form
     uint2* qr = x_q ? reinterpret_cast<uint2*>(x_q + row * K) : nullptr;
     for (int u = tid; u < (int)(Kp >> 4); u += kRowsThreads) {
-      int q[16];
+      uint32_t w[4];
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
         const int v = 2 * u + hv;
         if (v < V) {
-          float xf[8], gf[8];
-          unpack8(lds128(xb + 16 * v), xf);
-          unpack8(lds128(gbuf + 16 * v), gf);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) q[8 * hv + j] = row_code(__fmul_rn(xf[j], gf[j]), rq);
-          if (qr) {
-            uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              w0 |= (uint32_t)(q[8 * hv + j] & 0xff) << (8 * j);
-              w1 |= (uint32_t)(q[8 * hv + j + 4] & 0xff) << (8 * j);
-            }
-            qr[v] = make_uint2(w0, w1);
-          }
+          const uint4 xw = lds128(xb + 16 * v), gw = lds128(gbuf + 16 * v);
+          uint32_t w2[2];
+          row_codes<8>([&](int j) { return __fmul_rn(bf16_at(xw, j), bf16_at(gw, j)); }, rq, w2);
+          w[2 * hv] = w2[0];
+          w[2 * hv + 1] = w2[1];
+          if (qr) qr[v] = make_uint2(w2[0], w2[1]);
         } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) q[8 * hv + j] = 0;     // padding up to Kp: zero operands
+          w[2 * hv] = w[2 * hv + 1] = 0u;            // padding up to Kp: zero operands
         }
       }
-      if (x_ops) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, q);
+      if (x_ops) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, w);
     }
     __syncthreads();                               // buffer b is free for the row after next
   }

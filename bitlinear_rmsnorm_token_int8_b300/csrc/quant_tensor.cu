@@ -73,33 +73,23 @@ per_tensor_codes_kernel(const uint4* __restrict__ x, int64_t M, int K, const flo
     if (threadIdx.x == 0) act_scale[row] = sigma;
     uint2* qr = x_q ? reinterpret_cast<uint2*>(x_q + row * K) : nullptr;
     for (int u = threadIdx.x; u < (int)(Kp >> 4); u += kPtThreads) {
-      int q[16];
+      uint32_t w[4];
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
         const int v = 2 * u + hv;
+        w[2 * hv] = w[2 * hv + 1] = 0u;              // padding up to Kp: zero operands
         if (v < V) {
           float xf[8];
           unpack8(__ldcg(x + row * V + v), xf);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float t = fminf(fmaxf(__fdiv_rn(__fmul_rn(xf[j], 128.0f), d), -128.0f), 127.0f);
-            q[8 * hv + j] = (int)rintf(t);
+            w[2 * hv + (j >> 2)] |= (uint32_t)((int)rintf(t) & 0xff) << (8 * (j & 3));
           }
-          if (qr) {
-            uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              w0 |= (uint32_t)(q[8 * hv + j] & 0xff) << (8 * j);
-              w1 |= (uint32_t)(q[8 * hv + j + 4] & 0xff) << (8 * j);
-            }
-            qr[v] = make_uint2(w0, w1);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) q[8 * hv + j] = 0;     // padding up to Kp: zero operands
+          if (qr) qr[v] = make_uint2(w[2 * hv], w[2 * hv + 1]);
         }
       }
-      if (x_ops) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, q);
+      if (x_ops) write_act_ops16_any(x_ops, M, row, (int64_t)u << 4, Kp, w);
     }
   }
 }
