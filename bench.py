@@ -286,7 +286,7 @@ def traffic_record(workload, kernel_srcs):
 def kernel_sources():
     csrc = os.path.join(ROOT, "bitlinear_rmsnorm_token_int8_b300", "csrc")
     return [os.path.join(csrc, f) for f in ("decode_cc.cu", "decode_dp4a.cu", "quant_math.cuh", "decode_tc.cu",
-                                            "device_util.cuh")]
+                                            "device_util.cuh", "act_ops.cuh")]
 
 
 def timed_replays(torch, graph, stream, steps):
