@@ -18,7 +18,8 @@
 // 128-token tiles double the number of tiles where 256-token ones would leave
 // many SMs idle (a few hundred tokens, or a last wave at most half full); the
 // operand layout is the same (a 128-token tile reads half of a 256-token block).
-// Roles (448 threads):
+// Roles (512 threads, warpgroup-aligned so that setmaxnreg can move registers
+// from the producer and decoder warpgroups to the epilogue ones):
 //   warp 0      producer: per 512-k segment, one bulk copy of the tile's packed
 //               weights (up to 16 KB, the tile-major layout); per 128-k step,
 //               one bulk copy per operand plane of the token tile's block (or half),
@@ -27,15 +28,17 @@
 //               request, and per 128-byte row for tensor-map boxes.
 //   warp 1      allocates TMEM (512 columns: D = TT, A = 2 x 128 at 256); one lane
 //               issues the MMAs: per 128-k step, 4 k32 steps x 2 planes.
-//   warps 2-5   decoders: thread = weight row; 2-bit codes -> e4m3 bytes by
+//   warps 2-3   idle (the rest of the first warpgroup).
+//   warps 4-7   decoders: thread = weight row; 2-bit codes -> e4m3 bytes by
 //               byte permutes, written to TMEM as the A operand (tcgen05.st),
 //               128 columns per segment, double buffered.
-//   warps 6-13  epilogue: two warps per TMEM lane quarter, each taking half of
-//               the tile's tokens; tcgen05.ld of the accumulators (one chunk of
-//               32 tokens ahead), exact int32, y = fl(fl(acc * act_scale[m]) *
-//               w_scale[n]), stores.  The scales are loaded before the wait for
-//               the accumulators: the epilogue is the part of a tile that the
-//               MMAs of the next tile wait for.
+//   warps 8-15  epilogue: two warps per TMEM lane quarter (warpgroups 2 and 3),
+//               each taking half of the tile's tokens.  A warp loads all its
+//               accumulators (tcgen05.ld, up to 4 x 32 columns) into registers
+//               and releases them at once, so that the MMAs of the next tile run
+//               while it forms y = fl(fl(acc * act_scale[m]) * w_scale[n]) and
+//               stores (measured: the MMA warp had stalled about 6 us per tile
+//               for an epilogue that held the accumulators through its stores).
 // Weights reach the tensor core through TMEM rather than shared memory: the
 // decode expands 2 bits to 8, and TMEM takes those writes without costing
 // shared-memory bandwidth.
@@ -61,7 +64,12 @@ namespace {
 
 constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
 constexpr int kBlockT = 256;                // tokens per block of the operand layout
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;               // four warpgroups (see the roles above)
+// Registers per thread of each warpgroup after setmaxnreg: the launch gives every
+// thread 128 (the kernel is compiled to exactly that, checked before launch), and
+// the split must not exceed that total (128 x (56 + 104) + 256 x 176 = 512 x 128).
+constexpr uint32_t kRegsCtl = 56, kRegsDec = 104, kRegsEpi = 176;
+static_assert(128 * (kRegsCtl + kRegsDec) + 256 * kRegsEpi == kThreads * 128, "register split");
 constexpr int kNSXMax = 6;                  // operand stages (128 k each): 3 x 64 KB or 6 x 32 KB
 constexpr int kNSW = 2;                     // weight stages (512 k each)
 constexpr int kXBytes = 3 * 2 * kBlockT * 128;  // 192 KB of operand stages for either tile
@@ -187,101 +195,107 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   const int ctiles = nwbg * p.ntok;
   constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int ws = 0, xs = 0;
-      bool waited = false;
-      for (int ct = cid; ct < ctiles && !s_abort; ct += ncl) {
-        const int wb = (ct % nwbg) * CL + rank, tt = ct / nwbg;
-        for (int sg = 0; sg < nseg && !s_abort; ++sg) {
-          // weights of this segment
-          const int wslot = ws % kNSW, wround = ws / kNSW;
-          if (wround >= 1 && !wait_or_abort(B.empty_w + 8 * wslot, (wround - 1) & 1, &s_abort, p.dev_err))
-            break;
-          // the tile's rows of this segment: one contiguous block of the packed layout
-          const int rows = max(0, min(128, 16 * p.ntiles_n16 - wb * 128));
-          mbar_arrive_expect_tx(B.full_w + 8 * wslot, (uint32_t)(rows * 128));
-          if (rows > 0)
-            bulk_g2s(sbase + kOffW + wslot * kWStageBytes,
-                     p.packed + (int64_t)wb * nseg * 16384 + (int64_t)sg * rows * 128, (uint32_t)(rows * 128),
-                     B.full_w + 8 * wslot);
-          ++ws;
-          if (!waited) {                           // operands come from the previous kernel
-            pdl_wait();
-            waited = true;
-          }
-          for (int kk = 0; kk < 4; ++kk) {
-            const int xslot = xs % kNSX, xround = xs / kNSX;
-            if (xround >= 1 && !wait_or_abort(B.empty_x + 8 * xslot, (xround - 1) & 1, &s_abort, p.dev_err))
+  // Each warpgroup's branch starts with its register count: fewer for the
+  // producer/MMA and decoder warpgroups, more for the epilogue's.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        int ws = 0, xs = 0;
+        bool waited = false;
+        for (int ct = cid; ct < ctiles && !s_abort; ct += ncl) {
+          const int wb = (ct % nwbg) * CL + rank, tt = ct / nwbg;
+          for (int sg = 0; sg < nseg && !s_abort; ++sg) {
+            // weights of this segment
+            const int wslot = ws % kNSW, wround = ws / kNSW;
+            if (wround >= 1 && !wait_or_abort(B.empty_w + 8 * wslot, (wround - 1) & 1, &s_abort, p.dev_err))
               break;
-            mbar_arrive_expect_tx(B.full_x + 8 * xslot, (uint32_t)kXStageBytes);
-            const uint32_t part = kXPlaneBytes / CL;            // this CTA's rows of the block
-            const uint32_t dst = sbase + kOffX + xslot * kXStageBytes + rank * part;
-            const int blk = tt / kTilesPerBlock, sub = tt % kTilesPerBlock;
-            const uint8_t* src = p.x_ops + (((int64_t)blk * (nseg * 4) + sg * 4 + kk) << 15) +
-                                 sub * kXPlaneBytes + rank * part;
-            if (CL > 1) {
-              bulk_g2s_mc(dst, src, part, B.full_x + 8 * xslot, kMask);
-              bulk_g2s_mc(dst + kXPlaneBytes, src + p.plane_bytes, part, B.full_x + 8 * xslot, kMask);
-            } else {
-              bulk_g2s(dst, src, part, B.full_x + 8 * xslot);
-              bulk_g2s(dst + kXPlaneBytes, src + p.plane_bytes, part, B.full_x + 8 * xslot);
+            // the tile's rows of this segment: one contiguous block of the packed layout
+            const int rows = max(0, min(128, 16 * p.ntiles_n16 - wb * 128));
+            mbar_arrive_expect_tx(B.full_w + 8 * wslot, (uint32_t)(rows * 128));
+            if (rows > 0)
+              bulk_g2s(sbase + kOffW + wslot * kWStageBytes,
+                       p.packed + (int64_t)wb * nseg * 16384 + (int64_t)sg * rows * 128, (uint32_t)(rows * 128),
+                       B.full_w + 8 * wslot);
+            ++ws;
+            if (!waited) {                           // operands come from the previous kernel
+              pdl_wait();
+              waited = true;
             }
-            ++xs;
+            for (int kk = 0; kk < 4; ++kk) {
+              const int xslot = xs % kNSX, xround = xs / kNSX;
+              if (xround >= 1 && !wait_or_abort(B.empty_x + 8 * xslot, (xround - 1) & 1, &s_abort, p.dev_err))
+                break;
+              mbar_arrive_expect_tx(B.full_x + 8 * xslot, (uint32_t)kXStageBytes);
+              const uint32_t part = kXPlaneBytes / CL;            // this CTA's rows of the block
+              const uint32_t dst = sbase + kOffX + xslot * kXStageBytes + rank * part;
+              const int blk = tt / kTilesPerBlock, sub = tt % kTilesPerBlock;
+              const uint8_t* src = p.x_ops + (((int64_t)blk * (nseg * 4) + sg * 4 + kk) << 15) +
+                                   sub * kXPlaneBytes + rank * part;
+              if (CL > 1) {
+                bulk_g2s_mc(dst, src, part, B.full_x + 8 * xslot, kMask);
+                bulk_g2s_mc(dst + kXPlaneBytes, src + p.plane_bytes, part, B.full_x + 8 * xslot, kMask);
+              } else {
+                bulk_g2s(dst, src, part, B.full_x + 8 * xslot);
+                bulk_g2s(dst + kXPlaneBytes, src + p.plane_bytes, part, B.full_x + 8 * xslot);
+              }
+              ++xs;
+            }
           }
         }
+        if (!waited) pdl_wait();
+        // nothing may still be landing in shared memory when the CTA exits
+        for (int s = 0; s < kNSX && s < xs; ++s) {
+          const int last = xs - 1 - ((xs - 1 - s) % kNSX);
+          if (!mbar_wait_bounded(B.full_x + 8 * s, (last / kNSX) & 1, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+        }
+        for (int s = 0; s < kNSW && s < ws; ++s) {
+          const int last = ws - 1 - ((ws - 1 - s) % kNSW);
+          if (!mbar_wait_bounded(B.full_w + 8 * s, (last / kNSW) & 1, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+        }
       }
-      if (!waited) pdl_wait();
-      // nothing may still be landing in shared memory when the CTA exits
-      for (int s = 0; s < kNSX && s < xs; ++s) {
-        const int last = xs - 1 - ((xs - 1 - s) % kNSX);
-        if (!mbar_wait_bounded(B.full_x + 8 * s, (last / kNSX) & 1, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
-      }
-      for (int s = 0; s < kNSW && s < ws; ++s) {
-        const int last = ws - 1 - ((ws - 1 - s) % kNSW);
-        if (!mbar_wait_bounded(B.full_w + 8 * s, (last / kNSW) & 1, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      const uint32_t idesc = idesc_e4m3_f32(kTileW, TT);
-      int xs = 0, as = 0, tcount = 0;
-      for (int ct = cid; ct < ctiles && !s_abort; ct += ncl, ++tcount) {
-        if (tcount >= 1 && !wait_or_abort(B.d_empty, (tcount - 1) & 1, &s_abort, p.dev_err)) break;
-        tc_fence_after();
-        bool first = true;
-        for (int sg = 0; sg < nseg && !s_abort; ++sg) {
-          const int ab = as & 1;
-          if (!wait_or_abort(B.a_full + 8 * ab, (as >> 1) & 1, &s_abort, p.dev_err)) break;
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issue
+      if (lane == 0) {
+        const uint32_t idesc = idesc_e4m3_f32(kTileW, TT);
+        int xs = 0, as = 0, tcount = 0;
+        for (int ct = cid; ct < ctiles && !s_abort; ct += ncl, ++tcount) {
+          if (tcount >= 1 && !wait_or_abort(B.d_empty, (tcount - 1) & 1, &s_abort, p.dev_err)) break;
           tc_fence_after();
-          for (int kk = 0; kk < 4; ++kk) {
-            const int xslot = xs % kNSX;
-            if (!wait_or_abort(B.full_x + 8 * xslot, (xs / kNSX) & 1, &s_abort, p.dev_err)) break;
+          bool first = true;
+          for (int sg = 0; sg < nseg && !s_abort; ++sg) {
+            const int ab = as & 1;
+            if (!wait_or_abort(B.a_full + 8 * ab, (as >> 1) & 1, &s_abort, p.dev_err)) break;
             tc_fence_after();
-            const uint32_t xh = sbase + kOffX + xslot * kXStageBytes, xl = xh + kXPlaneBytes;
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              const uint32_t a = tmem + kColA + ab * 128 + kk * 32 + s * 8;
-              mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xh + 32 * s), idesc, first ? 0u : 1u);
-              mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xl + 32 * s), idesc, 1u);
-              first = false;
+            for (int kk = 0; kk < 4; ++kk) {
+              const int xslot = xs % kNSX;
+              if (!wait_or_abort(B.full_x + 8 * xslot, (xs / kNSX) & 1, &s_abort, p.dev_err)) break;
+              tc_fence_after();
+              const uint32_t xh = sbase + kOffX + xslot * kXStageBytes, xl = xh + kXPlaneBytes;
+  #pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                const uint32_t a = tmem + kColA + ab * 128 + kk * 32 + s * 8;
+                mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xh + 32 * s), idesc, first ? 0u : 1u);
+                mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xl + 32 * s), idesc, 1u);
+                first = false;
+              }
+              if (CL > 1) mma_commit_mc(B.empty_x + 8 * xslot, kMask);   // frees the stage in every CTA
+              else mma_commit(B.empty_x + 8 * xslot);
+              ++xs;
             }
-            if (CL > 1) mma_commit_mc(B.empty_x + 8 * xslot, kMask);   // frees the stage in every CTA
-            else mma_commit(B.empty_x + 8 * xslot);
-            ++xs;
+            mma_commit(B.a_empty + 8 * ab);           // frees the A buffer
+            ++as;
           }
-          mma_commit(B.a_empty + 8 * ab);           // frees the A buffer
-          ++as;
+          mma_commit(B.d_full);                       // accumulators complete
         }
-        mma_commit(B.d_full);                       // accumulators complete
+        // before TMEM is freed every MMA issued here must be finished
+        mma_commit(B.fin);
+        if (!mbar_wait_bounded(B.fin, 0, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
       }
-      // before TMEM is freed every MMA issued here must be finished
-      mma_commit(B.fin);
-      if (!mbar_wait_bounded(B.fin, 0, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
     }
-  } else if (warp < 6) {
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDec));
     // ------------------------------------------------------------ decoders
     const int q4 = warp & 3;                   // TMEM lane quarter of this warp
     const int r = 32 * q4 + lane;              // weight row within the block
@@ -328,10 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       }
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
     // ------------------------------------------------------------ epilogue
     pdl_wait();                                // act_scale and y follow the stream order
     const int q4 = warp & 3;
-    const int half = (warp - 6) >> 2;          // tokens [TT/2 half, TT/2 (half + 1)) of the tile
+    const int half = (warp - 8) >> 2;          // tokens [TT/2 half, TT/2 (half + 1)) of the tile
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
     constexpr int kChunks = TT / 2 / 32;       // chunks of 32 tokens per warp
     const int out_mode = p.out_dtype;
@@ -350,12 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       }
       if (!warp_wait_or_abort(B.d_full, tcount & 1, &s_abort, p.dev_err)) break;
       tc_fence_after();
-      uint32_t rv[2][32];
-      tmem_ld32(tmem + lane_addr + half * (TT / 2), rv[0]);
+      uint32_t rv[kChunks][32];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) tmem_ld32(tmem + lane_addr + half * (TT / 2) + 32 * c, rv[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.d_empty);   // accumulators may be overwritten
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
-        tmem_wait_ld();
-        if (c + 1 < kChunks) tmem_ld32(tmem + lane_addr + half * (TT / 2) + 32 * (c + 1), rv[(c + 1) & 1]);
         const int mbase = m0 + 32 * c;
         const int jmax = nv ? min(32, p.M - mbase) : 0;       // tokens of this chunk that exist
         const size_t o0 = (size_t)mbase * p.N + n;
@@ -364,14 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float as = __shfl_sync(0xffffffffu, as_lane[c], j);
-            if (j < jmax) yb[(size_t)j * p.N] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(__uint_as_float(rv[c & 1][j]), as), wsn));
+            if (j < jmax) yb[(size_t)j * p.N] = __float2bfloat16_rn(__fmul_rn(__fmul_rn(__uint_as_float(rv[c][j]), as), wsn));
           }
         } else if (out_mode == 0) {                          // fp32
           float* yf = reinterpret_cast<float*>(p.y) + o0;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float as = __shfl_sync(0xffffffffu, as_lane[c], j);
-            if (j < jmax) yf[(size_t)j * p.N] = __fmul_rn(__fmul_rn(__uint_as_float(rv[c & 1][j]), as), wsn);
+            if (j < jmax) yf[(size_t)j * p.N] = __fmul_rn(__fmul_rn(__uint_as_float(rv[c][j]), as), wsn);
           }
         } else {                                             // bf16 residual add
           __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o0;
@@ -392,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
               const int j = 16 * hh + jj;
               const float as = __shfl_sync(0xffffffffu, as_lane[c], j);
               if (j < jmax) {
-                const float yv = __fmul_rn(__fmul_rn(__uint_as_float(rv[c & 1][j]), as), wsn);
+                const float yv = __fmul_rn(__fmul_rn(__uint_as_float(rv[c][j]), as), wsn);
                 yb[(size_t)j * p.N] = __float2bfloat16_rn(__fadd_rn(res[jj], yv));
               }
             }
@@ -401,12 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
         if (p.acc_debug) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < jmax) p.acc_debug[o0 + (size_t)j * p.N] = (int32_t)__uint_as_float(rv[c & 1][j]);
+            if (j < jmax) p.acc_debug[o0 + (size_t)j * p.N] = (int32_t)__uint_as_float(rv[c][j]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B.d_empty);   // accumulators may be overwritten
     }
   }
   tc_fence_before();
@@ -488,6 +503,11 @@ cudaError_t launch_prefill_tc(const uint8_t* x_ops, const float* act_scale, cons
                     (void*)prefill_tc_kernel<1, 128>, (void*)prefill_tc_kernel<2, 128>}) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
+      // setmaxnreg moves registers within what the launch gave: 128 per thread
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, f);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
     }
     attr_set = true;
   }
