@@ -392,6 +392,7 @@ def test_forward_from_quant_operands_matches_oracle(M, N, K, dt, pdl):
     # 256-token tiles (enough tiles for whole waves)
     (256, 19200, 512, torch.bfloat16),  # 75 cluster tiles on 74 clusters
     (300, 13824, 512, torch.float32),   # 108 cluster tiles, the second token tile ragged
+    (38400, 128, 512, torch.bfloat16),  # one weight block: clusters of one, 150 tiles of 256 tokens
 ])
 def test_prefill_matches_oracle(M, N, K, dt):
     # M > 32 tokens run on the tcgen05 kernel (weights decoded into tensor memory)
