@@ -30,7 +30,10 @@
 //               The weight copies of the first NS stages are issued before the
 //               wait for the previous kernel, and the decoders start on them.
 //   warp 1      allocates 256 TMEM columns (A slots at 0, 64, 128; D at 192),
-//               one lane issues 8 MMAs per half segment (256 k) and commits.
+//               and issues 8 MMAs per half segment (256 k) and commits: the
+//               whole warp runs the loop and one elected lane issues (at
+//               n = 2 Mt <= 64 an MMA costs the issuing loop, not the tensor
+//               pipe: a one-lane loop took about three times as long).
 //   warps 2-5   decoders, thread = weight row: 2-bit codes -> e4m3 bytes by
 //               byte permutes (kCodeToE4M3), 64 TMEM columns per half segment
 //               (tcgen05.st), three A slots in rotation; afterwards the same
@@ -232,40 +235,49 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeTcPa
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      const uint32_t idesc = idesc_e4m3_f32(kRows, Nmma);
-      int a = 0;
-      bool first = true, ok = true;
-      for (int st = 0; st < nst && ok && !*s_abort; ++st) {
-        const int slot = st % p.NS;
-        if (!lane_wait(fullx0 + 8 * slot, (st / p.NS) & 1, s_abort, p.dev_err)) break;
-        const int sg = s0 + st * p.G, gc = min(p.G, s1 - sg);
-        const uint32_t xs = sbase + slot * p.stage_bytes + (uint32_t)(kWStageBytes * p.G);
-        for (int g = 0; g < gc && ok; ++g) {
-          for (int h = 0; h < 2; ++h) {
-            const int as = a % kASlots;
-            if (!lane_wait(afull0 + 8 * as, (a / kASlots) & 1, s_abort, p.dev_err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {    // k32 steps of this half segment
-              const uint32_t b = xs + g * kXSeg + (2 * h + (s >> 2)) * kXBlock + 32 * (s & 3);
-              mma_f8f6f4_ts(tmem + kColD, tmem + as * 64 + 8 * s, smem_desc_sw128(b), idesc, first ? 0u : 1u);
-              first = false;
-            }
-            mma_commit(aempty0 + 8 * as);    // the A slot may be rewritten
-            ++a;
+    // The whole warp runs the loop (its waits and descriptors are warp-uniform);
+    // one elected lane, the same throughout, issues every MMA and commit.
+    const uint32_t idesc = idesc_e4m3_f32(kRows, Nmma);
+    int a = 0;
+    bool first = true, ok = true;
+    for (int st = 0; st < nst && ok && !warp_aborted(s_abort); ++st) {
+      const int slot = st % p.NS;
+      if (!warp_wait(fullx0 + 8 * slot, (st / p.NS) & 1, s_abort, p.dev_err)) break;
+      const int sg = s0 + st * p.G, gc = min(p.G, s1 - sg);
+      const uint32_t xs = sbase + slot * p.stage_bytes + (uint32_t)(kWStageBytes * p.G);
+      for (int g = 0; g < gc && ok; ++g) {
+        for (int h = 0; h < 2; ++h) {
+          const int as = a % kASlots;
+          if (!warp_wait(afull0 + 8 * as, (a / kASlots) & 1, s_abort, p.dev_err)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {      // k32 steps of this half segment
+            const uint32_t b = xs + g * kXSeg + (2 * h + (s >> 2)) * kXBlock + 32 * (s & 3);
+            if (elect_one())
+              mma_f8f6f4_ts(tmem + kColD, tmem + as * 64 + 8 * s, smem_desc_sw128(b), idesc, first ? 0u : 1u);
+            __syncwarp();
+            first = false;
+          }
+          if (elect_one()) mma_commit(aempty0 + 8 * as);    // the A slot may be rewritten
+          __syncwarp();
+          ++a;
         }
-        if (ok) mma_commit(empty0 + 8 * slot);   // the stage's operands are read
       }
-      mma_commit(dfull);                     // accumulators complete
-      // before TMEM is freed every MMA issued here must be finished
-      mma_commit(fin);
-      if (!mbar_wait_bounded(fin, 0, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+      if (ok) {
+        if (elect_one()) mma_commit(empty0 + 8 * slot);     // the stage's operands are read
+        __syncwarp();
+      }
     }
+    if (elect_one()) {
+      mma_commit(dfull);                     // accumulators complete
+      mma_commit(fin);                       // before TMEM is freed every MMA issued here must be finished
+    }
+    __syncwarp();
+    if (lane == 0 && !mbar_wait_bounded(fin, 0, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ decoders
     const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;

@@ -194,6 +194,21 @@ __device__ __forceinline__ void mma_f8f6f4_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// True in one lane of the (converged) warp, the same lane at every call from the
+// same converged state.  A loop that the whole warp runs, issuing each MMA under
+// this predicate, issues small MMAs several times faster than the same loop run
+// by one lane under a lane-index branch (measured: about 18 against 50-70 cycles
+// per m128 n16 k32 MMA).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Arrives once on `bar` when all MMAs issued so far by this thread are done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
