@@ -26,8 +26,9 @@
 //               already in the swizzled layout the MMA reads (act_ops.cuh).
 //               Copies are few and large because the copy engine's cost is per
 //               request, and per 128-byte row for tensor-map boxes.
-//   warp 1      allocates TMEM (512 columns: D = TT, A = 2 x 128 at 256); one lane
-//               issues the MMAs: per 128-k step, 4 k32 steps x 2 planes.
+//   warp 1      allocates TMEM (512 columns: D = TT, A = 2 x 128 at 256) and
+//               issues the MMAs, per 128-k step 4 k32 steps x 2 planes: the whole
+//               warp runs the loop and one elected lane issues.
 //   warps 2-3   idle (the rest of the first warpgroup).
 //   warps 4-7   decoders: thread = weight row; 2-bit codes -> e4m3 bytes by
 //               byte permutes, written to TMEM as the A operand (tcgen05.st),
@@ -257,42 +258,53 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issue
-      if (lane == 0) {
-        const uint32_t idesc = idesc_e4m3_f32(kTileW, TT);
-        int xs = 0, as = 0, tcount = 0;
-        for (int ct = cid; ct < ctiles && !s_abort; ct += ncl, ++tcount) {
-          if (tcount >= 1 && !wait_or_abort(B.d_empty, (tcount - 1) & 1, &s_abort, p.dev_err)) break;
+      // The whole warp runs the loop (warp-uniform waits and descriptors); one
+      // elected lane, the same throughout, issues every MMA and commit.
+      const uint32_t idesc = idesc_e4m3_f32(kTileW, TT);
+      int xs = 0, as = 0, tcount = 0;
+      auto aborted = [&]() { return __any_sync(0xffffffffu, s_abort != 0); };
+      for (int ct = cid; ct < ctiles && !aborted(); ct += ncl, ++tcount) {
+        if (tcount >= 1 && !warp_wait_or_abort(B.d_empty, (tcount - 1) & 1, &s_abort, p.dev_err)) break;
+        tc_fence_after();
+        bool first = true;
+        for (int sg = 0; sg < nseg && !aborted(); ++sg) {
+          const int ab = as & 1;
+          if (!warp_wait_or_abort(B.a_full + 8 * ab, (as >> 1) & 1, &s_abort, p.dev_err)) break;
           tc_fence_after();
-          bool first = true;
-          for (int sg = 0; sg < nseg && !s_abort; ++sg) {
-            const int ab = as & 1;
-            if (!wait_or_abort(B.a_full + 8 * ab, (as >> 1) & 1, &s_abort, p.dev_err)) break;
+          for (int kk = 0; kk < 4; ++kk) {
+            const int xslot = xs % kNSX;
+            if (!warp_wait_or_abort(B.full_x + 8 * xslot, (xs / kNSX) & 1, &s_abort, p.dev_err)) break;
             tc_fence_after();
-            for (int kk = 0; kk < 4; ++kk) {
-              const int xslot = xs % kNSX;
-              if (!wait_or_abort(B.full_x + 8 * xslot, (xs / kNSX) & 1, &s_abort, p.dev_err)) break;
-              tc_fence_after();
-              const uint32_t xh = sbase + kOffX + xslot * kXStageBytes, xl = xh + kXPlaneBytes;
-  #pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                const uint32_t a = tmem + kColA + ab * 128 + kk * 32 + s * 8;
+            const uint32_t xh = sbase + kOffX + xslot * kXStageBytes, xl = xh + kXPlaneBytes;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const uint32_t a = tmem + kColA + ab * 128 + kk * 32 + s * 8;
+              if (elect_one()) {
                 mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xh + 32 * s), idesc, first ? 0u : 1u);
                 mma_f8f6f4_ts(tmem, a, smem_desc_sw128(xl + 32 * s), idesc, 1u);
-                first = false;
               }
+              __syncwarp();
+              first = false;
+            }
+            if (elect_one()) {
               if (CL > 1) mma_commit_mc(B.empty_x + 8 * xslot, kMask);   // frees the stage in every CTA
               else mma_commit(B.empty_x + 8 * xslot);
-              ++xs;
             }
-            mma_commit(B.a_empty + 8 * ab);           // frees the A buffer
-            ++as;
+            __syncwarp();
+            ++xs;
           }
-          mma_commit(B.d_full);                       // accumulators complete
+          if (elect_one()) mma_commit(B.a_empty + 8 * ab);           // frees the A buffer
+          __syncwarp();
+          ++as;
         }
-        // before TMEM is freed every MMA issued here must be finished
-        mma_commit(B.fin);
-        if (!mbar_wait_bounded(B.fin, 0, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+        if (elect_one()) mma_commit(B.d_full);                       // accumulators complete
+        __syncwarp();
       }
+      // before TMEM is freed every MMA issued here must be finished
+      if (elect_one()) mma_commit(B.fin);
+      __syncwarp();
+      if (lane == 0 && !mbar_wait_bounded(B.fin, 0, kSpin)) atomicCAS(p.dev_err, 0, kDevErrTimeout);
+      __syncwarp();
     }
   } else if (warp < 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDec));
