@@ -783,7 +783,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="layers of the workload (default: its own)")
     ap.add_argument("--ref-seconds", type=float, default=12.0, help="CPU oracle seconds per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+    ap.add_argument("--min-warmup-s", type=float, default=2.0,
                     help="warm-up replays continue at least this long (clock ramp-up; 0 under a profiler)")
     ap.add_argument("--headline-only", action="store_true",
                     help="only the headline decode (no decode_2b, prefill or stack_2b objects)")

@@ -417,6 +417,42 @@ def test_prefill_matches_oracle(M, N, K, dt):
         check_output(r)
 
 
+@pytest.mark.parametrize("M,N,K,dt,rows,toks,step", [
+    # 75 cluster tiles on 74 clusters: one cluster takes a second tile
+    (256, 19200, 2048, torch.bfloat16, (18944, 19200), (0, 256), 1),
+    # 94 cluster tiles: a partial second round of 20
+    (256, 24064, 2048, torch.float32, (18944, 24064), (0, 256), 5),
+    # 80 cluster tiles of 256 tokens, M = 500: the second round's 6 in the ragged token tile
+    (500, 10240, 2048, torch.bfloat16, (8704, 10240), (256, 500), 3),
+])
+def test_prefill_partial_last_round_sampled(M, N, K, dt, rows, toks, step):
+    # More cluster tiles than clusters: the persistent grid's partial last round;
+    # every token of those tiles' rows (every step-th row) is compared, and a
+    # random sample of the rest.
+    seed = M + 5 * N + K
+    x = synth.activations(M, K, seed=seed)
+    g = synth.rms_gains(K, seed=seed + 1)
+    W = synth.latent_weights(N, K, seed=seed + 2)
+    packed, w_scale, gamma = bl.bitlinear_pack_weights(W.cuda())
+    xq, sc, ops = bl.bitlinear_quant_act(x.cuda(), g.cuda(), RMS_EPS, x_ops=True, flags=bl.FLAG_PDL)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    y = bl.bitlinear_forward(None, sc, packed, w_scale, out_dtype=dt, acc_debug=acc, x_ops=ops,
+                             flags=bl.FLAG_PDL, K=K)
+    torch.cuda.synchronize()
+    assert bl.bitlinear_get_device_error() == 0
+    o_xq, o_sig = oracle.act_quant(synth.bf16_bits(x), synth.bf16_bits(g), RMS_EPS)
+    o_packed, o_gamma, o_wq = oracle.pack_weights(W.numpy())
+    r = dict(y=y.cpu(), acc=acc.cpu().numpy(), xq=xq.cpu().numpy(),
+             packed=layout.canonical_from_tiled(packed.cpu().numpy(), N, K),
+             gamma=np.float32(gamma.cpu().item()), o_xq=o_xq, o_sig=o_sig, o_packed=o_packed,
+             o_gamma=o_gamma, o_wq=o_wq)
+    tt, nn = np.meshgrid(np.arange(*toks), np.arange(rows[0], rows[1], step), indexing="ij")
+    rng = np.random.default_rng(seed)
+    ts = np.concatenate([tt.ravel(), rng.integers(0, M, 4096), [0, M - 1]])
+    ns = np.concatenate([nn.ravel(), rng.integers(0, N, 4096), [0, N - 1]])
+    check_output(r, ts, ns)
+
+
 def test_forward_exact_at_accumulator_extremes():
     # every partial sum at its largest magnitude: all codes +-127 against all-(+1) / all-(-1)
     # rows, and alternating signs so that partial sums swing between large values

@@ -212,3 +212,30 @@ def test_layer_kernel_statistics_equal_the_quantization_kernels(K):
     # and the pair sum is the exact sum of squares rounded once, for these inputs
     exact = sum(int(v) for v in (x.astype(np.float64) ** 2 * 2.0 ** 300).astype(object))
     assert abs(float(s1) - float(np.float64(exact) * 2.0 ** -300)) <= np.spacing(s1)
+
+
+# ---------------------------------------------------------------------------
+# prefill_tc.cu: the persistent grid's cluster tiles (launch_prefill_tc and the
+# loops of the producers, decoders and epilogue)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,CL,TT", [
+    (256, 19200, 2, 256), (500, 10240, 2, 256), (2048, 14336, 2, 256), (2048, 4096, 2, 256),
+    (600, 512, 2, 128), (38400, 128, 1, 256), (4000, 1280, 1, 128), (1000, 9728, 2, 128), (33, 48, 1, 128)])
+def test_prefill_tiles_cover_every_row_and_token_once(M, N, CL, TT):
+    sms = 148
+    nwb = (N + 127) // 128
+    nwbg = (nwb + CL - 1) // CL                            # weight-block groups
+    ntok = (M + TT - 1) // TT
+    ctiles = nwbg * ntok
+    clusters = min(sms // CL, ctiles)
+    Mp = (M + 255) // 256 * 256
+    seen = np.zeros((nwbg * CL, Mp), dtype=np.int32)
+    for cid in range(clusters):                            # each cluster's persistent loop
+        for ct in range(cid, ctiles, clusters):
+            for rank in range(CL):
+                wb, tt = (ct % nwbg) * CL + rank, ct // nwbg
+                seen[wb, tt * TT:(tt + 1) * TT] += 1
+    assert (seen[:, :M] == 1).all()                        # every weight block and token once
+    assert (seen[:nwb, M:] <= 1).all()
+    assert clusters * CL <= sms
