@@ -439,10 +439,16 @@ DecodePlan decode_plan(int64_t M, int64_t N, int64_t K, int sms) {
   const int per_sm = pl.smem <= kTwoPerSm ? 2 : 1;
   const int64_t slots = (int64_t)per_sm * sms;
   // S: fewest segment-times, counting one segment of fixed cost per CTA and
-  // whole waves of `slots` CTAs; ties go to the smaller S.
+  // whole waves of `slots` CTAs; ties go to the smaller S.  A split leaves each
+  // CTA at least two segments: a cluster starts only when all of its CTAs find
+  // room in one GPC, which in a chain of launches overlapping by programmatic
+  // dependent launch delayed whole clusters by several microseconds, and with
+  // one segment per CTA that delay is not amortized (8B O projection, 16 tokens:
+  // 10.4 us in clusters of 8, 7.0 us in clusters of 4).
   int64_t best = -1;
   pl.S = 1;
   for (int S = 1; S <= kMaxSplit && S <= pl.nseg; ++S) {
+    if (S > 1 && (pl.nseg + S - 1) / S < 2) break;
     const int64_t ctas = (int64_t)pl.ntile * S;
     const int64_t waves = (ctas + slots - 1) / slots;
     const int64_t cost = waves * ((pl.nseg + S - 1) / S + 1);
