@@ -328,7 +328,8 @@ def bitlinear_linear_forward(x: torch.Tensor, gain, rms_eps: float, packed: torc
     ``gain``: RMSNorm weight (bf16 [K]) or None; ``rms_eps < 0`` skips RMSNorm.  ``x_q``
     (int8 [M,K]) and ``act_scale`` (fp32 [M]) receive the codes and scales when given.
     ``residual``: y (bf16) holds the residual on entry and receives y + result.
-    One token with K <= 8192 runs as a single kernel; :func:`bitlinear_linear_route`
+    One token with K <= 8192 (K <= 16384 for at least 12 MiB of packed weights) runs as a
+    single kernel; :func:`bitlinear_linear_route`
     tells which kernels a shape takes (the results are the same on every route).
     ``prefetch``: an L2 hint, typically the next call's packed weights (see
     :func:`bitlinear_forward`).

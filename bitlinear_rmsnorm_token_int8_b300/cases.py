@@ -8,7 +8,7 @@
         tokens, the tcgen05 prefill kernel above), `ops` (operand form only:
         always a tcgen05 kernel), `codes` (x_q only) or `layer` (the one-call
         layer bitlinear_linear_forward on the bf16 activations: for one token
-        with K <= 8192 a single kernel that also quantizes).
+        with K <= 8192, or up to 16384 for large matrices, a single kernel that also quantizes).
     python -m bitlinear_rmsnorm_token_int8_b300.cases shapes WORKLOAD [reps]
         every (tokens, projection) shape of a named workload (synth.WORKLOADS),
         `reps` launches each of the kernel bench.py times for it (route `layer`

@@ -36,7 +36,9 @@
 // quantizes the tokens itself with the thread-to-input mapping, per-thread
 // order and reduction tree of quant_act_kernel (thread u takes inputs
 // 16u..16u+15; the tree spans that kernel's warps, the others add nothing),
-// so codes and scales equal the separate quantization bit for bit.  Its token
+// so codes and scales equal the separate quantization bit for bit.  Rows of
+// more than 512 units (that kernel runs up to 1024 threads on them) take the
+// variant in which each thread plays two of its threads.  Its token
 // row arrives by one bulk copy into shared memory, through the copy engine
 // rather than behind the ring's first S items of 16-byte requests (8B gate+up
 // at one token: 12.8 -> 12.5-12.6 us per launch).
@@ -66,7 +68,7 @@ constexpr int kItemBytes = 32 * kCB * 16;      // one warp's item: 4 KB
 constexpr int kChunkPitch = 80;                // a staged 64-byte chunk + 16 bytes
 constexpr int kSegPitch = 8 * kChunkPitch;     // one token's 512 inputs in shared memory
 constexpr uint32_t kCodeToI8 = 0x00FF0100u;    // bytes 0x00 (code 0), 0x01 (+1), 0xFF (-1)
-constexpr int kFusedMaxK = 8192;               // layer form: quant_act_kernel's threads <= 512
+constexpr int kFusedMaxK = 16384;              // layer form: quant_act_kernel's threads <= 1024
 constexpr int64_t kSmemCap = 220 * 1024;       // dynamic shared memory budget per CTA
 constexpr uint32_t kSpin = 1u << 24;           // polls of a bounded mbarrier wait
 
@@ -134,7 +136,9 @@ __device__ __forceinline__ void dot_chunk(const uint4 w, uint32_t xs, uint32_t t
 
 // MT: tokens the kernel is compiled for (M <= MT).  KS: lanes per (row, chunk).
 // FUSED: the layer form (quantize x) instead of reading x_q.
-template <int MT, int KS, bool FUSED>
+// FUSED: 0 for the codes form; 1 or 2 for the layer form, the number of
+// quant_act_kernel threads each thread plays (2 for rows of more than 512 units).
+template <int MT, int KS, int FUSED>
 __global__ void __launch_bounds__(kCcThreads, 1) decode_cc_kernel(const DecodeCcParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ float s_max[MT][32];
@@ -199,14 +203,19 @@ __global__ void __launch_bounds__(kCcThreads, 1) decode_cc_kernel(const DecodeCc
 
   for (int n = 0; n < S; ++n) issue();       // weights: before the wait
 
-  uint4 gv[2];                               // the layer form's RMSNorm gain (not written by earlier kernels)
+  // the layer form's RMSNorm gain (not written by earlier kernels) of the units
+  // tid and tid + kCcThreads (quant_act_kernel's threads tid and tid + 512)
+  constexpr int kVT = FUSED > 1 ? 2 : 1;
+  uint4 gv[kVT][2];
   const int V = p.K >> 3, U = (V + 1) >> 1;
   if constexpr (FUSED) {
 #pragma unroll
-    for (int hv = 0; hv < 2; ++hv) {
-      const int v = 2 * tid + hv;
-      gv[hv] = (p.gain && tid < U && v < V) ? __ldg(p.gain + v) : kOnes;
-    }
+    for (int vt = 0; vt < kVT; ++vt)
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        const int u = tid + vt * kCcThreads, v = 2 * u + hv;
+        gv[vt][hv] = (p.gain && u < U && v < V) ? __ldg(p.gain + v) : kOnes;
+      }
   }
   if (warp == 0) l2_prefetch_share(p.pf, p.pf_bytes, lane, 32);
   pdl_launch_dependents();
@@ -224,53 +233,55 @@ __global__ void __launch_bounds__(kCcThreads, 1) decode_cc_kernel(const DecodeCc
     }
     x_landed = mbar_wait_bounded(xbar, 0, kSpin);
     if (!x_landed) atomicCAS(p.dev_err, 0, kDevErrTimeout);
-    // statistics of each token row as quant_act_kernel: thread u < U takes inputs
-    // 16u..16u+15 (vectors 2u, 2u + 1), in that order
-    uint4 xv[MT][2];
-    float amax[MT], hi[MT], lo[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      amax[m] = 0.0f;
-      hi[m] = 0.0f;
-      lo[m] = 0.0f;
+    // statistics of the token row (M = 1) as quant_act_kernel with p.Tq threads
+    // (up to 1024): its thread u < U takes inputs 16u..16u+15 (vectors 2u, 2u + 1),
+    // in that order; thread tid here plays its thread tid and, for rows of more
+    // than 512 units, its thread tid + 512 (warps warp and warp + 16 there).
+    static_assert(!FUSED || MT == 1, "the layer form takes one token");
+    constexpr bool two = kVT > 1;
+    // unit u's vectors into x, its statistics through that kernel's warp tree into slot
+    auto unit_stats = [&](int u, uint4 (&x)[2], const uint4 (&g)[2], int slot) {
+      float amax = 0.0f, hi = 0.0f, lo = 0.0f;
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
-        const int v = 2 * tid + hv;
-        if (m < p.M && tid < U && v < V) {
-          xv[m][hv] = lds128(xrow + 16 * v);
+        const int v = 2 * u + hv;
+        if (u < U && v < V) {
+          x[hv] = lds128(xrow + 16 * v);
           float xf[8], gf[8];
-          unpack8(xv[m][hv], xf);
-          unpack8(gv[hv], gf);
+          unpack8(x[hv], xf);
+          unpack8(g[hv], gf);
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            amax[m] = fmaxf(amax[m], fabsf(__fmul_rn(xf[jj], gf[jj])));
+            amax = fmaxf(amax, fabsf(__fmul_rn(xf[jj], gf[jj])));
             float s_, e_;
-            two_sum(hi[m], __fmul_rn(xf[jj], xf[jj]), s_, e_);   // x^2 is exact in fp32
-            hi[m] = s_;
-            lo[m] = __fadd_rn(lo[m], e_);
+            two_sum(hi, __fmul_rn(xf[jj], xf[jj]), s_, e_);   // x^2 is exact in fp32
+            hi = s_;
+            lo = __fadd_rn(lo, e_);
           }
         } else {
-          xv[m][hv] = make_uint4(0u, 0u, 0u, 0u);
+          x[hv] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      // the warp's xor tree, as block_stats
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        amax[m] = fmaxf(amax[m], __shfl_xor_sync(0xffffffffu, amax[m], o));
-        const float h2 = __shfl_xor_sync(0xffffffffu, hi[m], o), l2 = __shfl_xor_sync(0xffffffffu, lo[m], o);
-        pair_add(hi[m], lo[m], h2, l2);
+      for (int o = 16; o > 0; o >>= 1) {     // the warp's xor tree, as block_stats
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+        pair_add(hi, lo, h2, l2);
       }
       if (lane == 0) {
-        s_max[m][warp] = amax[m];
-        s_ss[m][warp] = make_float2(hi[m], lo[m]);
+        s_max[0][slot] = amax;
+        s_ss[0][slot] = make_float2(hi, lo);
       }
-    }
+    };
+    uint4 xv0[2], xv1[2];
+    unit_stats(tid, xv0, gv[0], warp);
+    if constexpr (two) unit_stats(tid + kCcThreads, xv1, gv[kVT - 1], warp + 16);
     __syncthreads();
-    // warp m: the tree over quant_act_kernel's p.Tq / 32 warps (zero beyond them)
+    // warp 0: the tree over that kernel's p.Tq / 32 warps (zero beyond them)
     const int nwq = p.Tq >> 5;
-    if (warp < MT && warp < p.M) {
-      float a = lane < nwq ? s_max[warp][lane] : 0.0f;
-      float2 p2 = lane < nwq ? s_ss[warp][lane] : make_float2(0.0f, 0.0f);
+    if (warp == 0) {
+      float a = lane < nwq ? s_max[0][lane] : 0.0f;
+      float2 p2 = lane < nwq ? s_ss[0][lane] : make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
@@ -278,33 +289,28 @@ __global__ void __launch_bounds__(kCcThreads, 1) decode_cc_kernel(const DecodeCc
         pair_add(p2.x, p2.y, h2, l2);
       }
       if (lane == 0) {
-        s_m[warp] = a;
-        s_sum[warp] = __fadd_rn(p2.x, p2.y);
+        s_m[0] = a;
+        s_sum[0] = __fadd_rn(p2.x, p2.y);
       }
     }
     __syncthreads();
-    // codes of this unit (zero past K and for tokens past M), staged permuted
-    if (tid < p.nseg * 32) {
-      const int s = tid >> 5, cc = (tid >> 2) & 7, jj = tid & 3;
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (m < p.M) {
-          const RowQuant rq = row_quant(s_m[m], s_sum[m], p.K, p.rms_eps);
-          row_codes<16>([&](int e) { return __fmul_rn(bf16_at(xv[m][e >> 3], e & 7), bf16_at(gv[e >> 3], e & 7)); },
-                        rq, w);
-          if (tid == 0) {
-            s_sigma[m] = rq.sigma;
-            if (blockIdx.x == 0 && p.act_scale_out) p.act_scale_out[m] = rq.sigma;
-          }
-        }
-        const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(xst + m * tstride + s * kSegPitch + cc * kChunkPitch + 16 * jj) =
-            permute16(codes);
-        if (blockIdx.x == 0 && p.x_q_out && m < p.M && tid < U)
-          *reinterpret_cast<uint4*>(p.x_q_out + (size_t)m * p.K + 16 * tid) = codes;
-      }
+    // codes of the units (zero past K), staged permuted
+    const RowQuant rq = row_quant(s_m[0], s_sum[0], p.K, p.rms_eps);
+    if (tid == 0) {
+      s_sigma[0] = rq.sigma;
+      if (blockIdx.x == 0 && p.act_scale_out) p.act_scale_out[0] = rq.sigma;
     }
+    auto unit_codes = [&](int u, const uint4 (&x)[2], const uint4 (&g)[2]) {
+      if (u >= p.nseg * 32) return;
+      const int sgm = u >> 5, cc = (u >> 2) & 7, jj = u & 3;
+      uint32_t w[4];
+      row_codes<16>([&](int e) { return __fmul_rn(bf16_at(x[e >> 3], e & 7), bf16_at(g[e >> 3], e & 7)); }, rq, w);
+      const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(xst + sgm * kSegPitch + cc * kChunkPitch + 16 * jj) = permute16(codes);
+      if (blockIdx.x == 0 && p.x_q_out && u < U) *reinterpret_cast<uint4*>(p.x_q_out + 16 * u) = codes;
+    };
+    unit_codes(tid, xv0, gv[0]);
+    if constexpr (two) unit_codes(tid + kCcThreads, xv1, gv[kVT - 1]);
   } else {
     const int groupsK = p.nseg * 32;         // 16-input groups per token (Kp / 16)
     for (int i = tid; i < MT * groupsK; i += kCcThreads) {
@@ -396,7 +402,7 @@ int cc_stages(int64_t M, int64_t K, int64_t extra = 0) {
   return 0;
 }
 
-template <int MT, int KS, bool FUSED>
+template <int MT, int KS, int FUSED>
 cudaError_t launch_cfg(const DecodeCcParams& p, int grid, size_t smem, bool pdl, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -418,7 +424,7 @@ cudaError_t launch_cfg(const DecodeCcParams& p, int grid, size_t smem, bool pdl,
   return cudaLaunchKernelEx(&cfg, decode_cc_kernel<MT, KS, FUSED>, p);
 }
 
-template <int MT, bool FUSED>
+template <int MT, int FUSED>
 cudaError_t launch_mt(const DecodeCcParams& p, int KS, int grid, size_t smem, bool pdl, cudaStream_t stream) {
   if (KS == 4) return launch_cfg<MT, 4, FUSED>(p, grid, smem, pdl, stream);
   if (KS == 2) return launch_cfg<MT, 2, FUSED>(p, grid, smem, pdl, stream);
@@ -445,10 +451,11 @@ cudaError_t launch_cc(DecodeCcParams& p, int64_t M, int64_t N, int64_t K, bool f
   const size_t smem = (size_t)kCcWarps * p.S * kItemBytes + (size_t)cc_staging(M, K) + (size_t)xrow_bytes;
   cudaError_t e;
   if (fused) {
-    e = launch_mt<1, true>(p, KS, grid, smem, pdl, stream);
+    e = p.Tq > kCcThreads ? launch_mt<1, 2>(p, KS, grid, smem, pdl, stream)
+                          : launch_mt<1, 1>(p, KS, grid, smem, pdl, stream);
   } else {
-    e = M <= 1 ? launch_mt<1, false>(p, KS, grid, smem, pdl, stream)
-               : launch_mt<2, false>(p, KS, grid, smem, pdl, stream);
+    e = M <= 1 ? launch_mt<1, 0>(p, KS, grid, smem, pdl, stream)
+               : launch_mt<2, 0>(p, KS, grid, smem, pdl, stream);
   }
   count_launches(1);
   return e;
@@ -465,12 +472,17 @@ bool codes_route(int64_t M, int64_t N, int64_t K) {
   return M >= 1 && M <= kCodesMaxM && cc_stages(M, K) > 0;
 }
 
-// The layer form: one token, whose quant_act_kernel row fits one CTA (K <= 8192).
+// The layer form: one token, whose quant_act_kernel row (up to 1024 threads) this
+// kernel's 512 threads can play (K <= 16384).
 // Measured in chains of dependent launches: for one token the in-kernel
 // quantization costs less than a separate quantization launch; for two it costs
 // more (8B gate+up at two tokens: 19.2 us as one kernel, 13.8 + ~3.5 us as two).
 bool fused_route(int64_t M, int64_t N, int64_t K) {
-  return M == 1 && codes_route(M, N, K) && K <= kFusedMaxK && cc_stages(M, K, 2 * K) > 0;
+  if (!(M == 1 && codes_route(M, N, K) && K <= kFusedMaxK && cc_stages(M, K, 2 * K) > 0)) return false;
+  // above 8192 inputs only this persistent kernel has a layer form (the small-CTA
+  // kernels of decode_dp4a.cu stop there), so smaller matrices keep the
+  // quantization + small-CTA codes kernel
+  return K <= 8192 || packed_layout_bytes(N, K) >= kCcMinBytes;
 }
 
 size_t decode_cc_smem(int64_t M, int64_t K) {

@@ -118,7 +118,8 @@ cudaError_t launch_codes_cc(const int8_t* x_q, const float* act_scale, const uin
                             L2Prefetch pf = {});
 
 // The whole layer (RMSNorm + quantization + contraction) for one token in one kernel,
-// when K <= 8192 and the codes route applies; x_q and act_scale outputs optional.
+// when the codes route applies and K <= 8192 (K <= 16384 for matrices of at least
+// kCcMinBytes); x_q and act_scale outputs optional.
 bool fused_route(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_layer_cc(const uint16_t* x, const uint16_t* gain, float rms_eps, const uint8_t* packed,
                             const float* w_scale, int64_t M, int64_t N, int64_t K, int out_dtype, void* y,

@@ -325,9 +325,10 @@ size_t bitlinear_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 /* Which kernels bitlinear_linear_forward launches for this shape (the results do
  * not depend on it):
  *   BITLINEAR_ROUTE_FUSED    one kernel: RMSNorm, quantization and the int8-code
- *                            contraction together (one token, K <= 8192);
+ *                            contraction together (one token, K <= 8192, or
+ *                            K <= 16384 for at least 12 MiB of packed weights);
  *   BITLINEAR_ROUTE_CODES    quantization to int8 codes, then the CUDA-core
- *                            contraction on them (one token with K > 8192, or
+ *                            contraction on them (one token with longer K, or
  *                            two tokens);
  *   BITLINEAR_ROUTE_DECODE   quantization to the operand form, then the tcgen05
  *                            decode contraction (3 to 32 tokens, or two where
@@ -358,8 +359,9 @@ int bitlinear_prefill_cluster_size(const void *x_ops, int64_t M, int64_t N, int6
 /*
  * The whole BitLinear layer in one call ([P4-code] BitLinear.forward: RMSNorm,
  * activation_quant, the ternary product and the rescale; [P1-impl]
- * bitlinear_forward(x, W_packed, s)).  For one token with K <= 8192 a single
- * kernel does all of it (BITLINEAR_ROUTE_FUSED); otherwise the call enqueues
+ * bitlinear_forward(x, W_packed, s)).  For one token with K <= 8192 (K <= 16384
+ * for at least 12 MiB of packed weights) a single kernel does all of it
+ * (BITLINEAR_ROUTE_FUSED); otherwise the call enqueues
  * bitlinear_quant_act into the workspace (int8 codes or the operand form), then
  * bitlinear_forward on it, the second launch overlapping the first (programmatic
  * dependent launch).  bitlinear_linear_route tells which.  Results equal those of

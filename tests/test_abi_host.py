@@ -63,7 +63,9 @@ def test_linear_route(L):
     route = L.bitlinear_linear_route
     assert route(1, 2560, 2560) == bl.ROUTE_FUSED            # one token, K <= 8192: one kernel
     assert route(1, 4096, 8192) == bl.ROUTE_FUSED
-    assert route(1, 4096, 14336) == bl.ROUTE_CODES           # longer K: quant + codes kernel
+    assert route(1, 4096, 14336) == bl.ROUTE_FUSED           # up to 16384 on the persistent kernel
+    assert route(1, 512, 14336) == bl.ROUTE_CODES            # a small matrix: quant + small-CTA codes kernel
+    assert route(1, 4096, 16896) == bl.ROUTE_CODES           # longer K: quant + codes kernel
     assert route(2, 3840, 2560) == bl.ROUTE_CODES            # two tokens: quant + codes kernel
     assert route(2, 28672, 4096) == bl.ROUTE_CODES
     assert route(2, 4096, 14336) == bl.ROUTE_CODES

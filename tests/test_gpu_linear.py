@@ -151,9 +151,11 @@ def test_linear_residual_and_pdl_chain(M):
 @pytest.mark.parametrize("M,K,N,gain,rms", [
     (1, 128, 144, True, True), (1, 1152, 272, False, True), (1, 2560, 3840, True, True),
     (1, 6912, 2560, True, False), (1, 8192, 400, True, True), (1, 4096, 28672, True, True),
-    (1, 2560, 13824, False, True)])
+    (1, 2560, 13824, False, True),
+    # K above 8192 (matrices of at least 12 MiB): two of the quantization's threads per thread
+    (1, 14336, 4096, True, True), (1, 10240, 5120, True, False), (1, 16384, 3200, False, True)])
 def test_linear_one_token_fused(M, K, N, gain, rms):
-    # one token, K <= 8192: RMSNorm, quantization and the contraction in one kernel.
+    # one token: RMSNorm, quantization and the contraction in one kernel.
     # Its codes, scales, accumulators and outputs equal the oracle's and, bit for bit, those
     # of the two-kernel path (quantization, then the contraction on the int8 codes)
     assert bl.bitlinear_linear_route(M, N, K) == bl.ROUTE_FUSED

@@ -136,14 +136,14 @@ _GOLDEN = json.load(open(os.path.join(os.path.dirname(os.path.abspath(__file__))
 
 @pytest.mark.parametrize("key", ["act_clamp_regular_tiny_row", "act_clamp_plain_tiny_row",
                                  "act_clamp_small_rmsnorm_row"])
-@pytest.mark.parametrize("kernel", ["one_row_per_cta", "many_rows", "one_token_layer"])
+@pytest.mark.parametrize("kernel", ["one_row_per_cta", "many_rows", "one_token_layer", "one_token_layer_long"])
 def test_quant_clamp_golden_rows_every_kernel(key, kernel):
     # activation_quant clamps the max of the RMSNorm output at 1e-8: the hand-worked rows
     # (zero-padded, which changes neither max|n| nor the rounding of mean(x^2) + eps)
     # through each kernel that quantizes
     ex = _GOLDEN[key]
     eps = RMS_EPS if ex["rms_eps"] >= 0 else -1.0
-    K = 4104 if kernel == "many_rows" else 512
+    K = {"many_rows": 4104, "one_token_layer_long": 14336}.get(kernel, 512)
     M = 600 if kernel == "many_rows" else 1
     rows = np.zeros((M, K), dtype=np.float32)
     rows[:, :8] = ex["x"]
@@ -151,8 +151,8 @@ def test_quant_clamp_golden_rows_every_kernel(key, kernel):
     x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     want = np.zeros((M, K), dtype=np.int8)
     want[:, :8] = ex["x_q"]
-    if kernel == "one_token_layer":
-        N = 128
+    if kernel.startswith("one_token_layer"):
+        N = 4096 if kernel == "one_token_layer_long" else 128    # the persistent kernel, two threads' units each
         assert bl.bitlinear_linear_route(1, N, K) == bl.ROUTE_FUSED
         packed, w_scale, _ = bl.bitlinear_pack_weights(synth.latent_weights(N, K, seed=5).cuda())
         xq = torch.empty((1, K), dtype=torch.int8, device="cuda")
