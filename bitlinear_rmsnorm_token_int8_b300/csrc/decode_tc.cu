@@ -445,13 +445,17 @@ DecodePlan decode_plan(int64_t M, int64_t N, int64_t K, int sms) {
   // dependent launch delayed whole clusters by several microseconds, and with
   // one segment per CTA that delay is not amortized (8B O projection, 16 tokens:
   // 10.4 us in clusters of 8, 7.0 us in clusters of 4).
+  // From 16 tokens a grid that puts two CTAs on some SMs costs 2.5 segments more
+  // (measured: 8B QKV at 16 tokens 8.2 us in 96 CTAs of four segments, 8.9 us in
+  // 192 CTAs of two; at 4 tokens the 192 CTAs win).  Costs in half segments.
+  const int64_t crowd = Mt >= 16 ? 5 : 0;
   int64_t best = -1;
   pl.S = 1;
   for (int S = 1; S <= kMaxSplit && S <= pl.nseg; ++S) {
     if (S > 1 && (pl.nseg + S - 1) / S < 2) break;
     const int64_t ctas = (int64_t)pl.ntile * S;
     const int64_t waves = (ctas + slots - 1) / slots;
-    const int64_t cost = waves * ((pl.nseg + S - 1) / S + 1);
+    const int64_t cost = 2 * waves * ((pl.nseg + S - 1) / S + 1) + (ctas > sms ? crowd : 0);
     if (best < 0 || cost < best) {
       best = cost;
       pl.S = S;
